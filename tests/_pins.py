@@ -1,0 +1,267 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+Each check takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with a value the pages print, a hand expansion, a closed
+form, a special case that reduces to a library routine, or the invariant the
+pages state (the parallel, recurrent and chunkwise forms give the same
+output).  test_oracle.py runs them on the real oracle; test_oracle_mutants.py
+runs them on copies with planted mistakes and expects at least one to fail.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = np.array([float(x) for x in rest])
+    return vals
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _all_forms(o, q, k, v, g, chunks=()):
+    """Outputs and final states of every form; chunkwise for each chunk size."""
+    res = {"parallel": (o.parallel(q, k, v, g), None)}
+    res["recurrent"] = o.recurrent(q, k, v, g)
+    for C in chunks:
+        res[f"chunk{C}"] = o.chunkwise(q, k, v, g, C)
+    return res
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    scale = max(np.max(np.abs(b)), 1e-300) if b.size else 1.0
+    err = np.max(np.abs(a - b)) / scale if a.size else 0.0
+    assert err <= tol, f"{what}: normalised error {err:.3e} > {tol:.1e}"
+
+
+# --- values the pages print ------------------------------------------------
+
+def check_gamma_printed(o):
+    """gamma_h = 1 - 2^(-5-h) (0-based h); the printed 0.996094 / ~177 tokens."""
+    gold = _read_golden("decay_half_life.txt")
+    assert o.gamma(0) == 0.96875 and o.gamma(1) == 0.984375
+    g3 = o.gamma(3)
+    assert g3 == 1.0 - 2.0 ** -8
+    assert round(g3, 6) == gold["gamma_printed"][0]
+    half_life = math.log(2.0) / -math.log(g3)
+    assert round(half_life) == gold["half_life_tokens_printed"][0]
+    hs = np.arange(16)
+    assert np.array_equal(o.gamma(hs), 1.0 - 2.0 ** (-5.0 - hs))
+
+
+# --- hand expansions ---------------------------------------------------------
+
+def check_hand_expanded_scalar(o):
+    gold = _read_golden("hand_expanded_n3.txt")
+    q = gold["q"].reshape(1, 1, 3, 1)
+    k = gold["k"].reshape(1, 1, 3, 1)
+    v = gold["v"].reshape(1, 1, 3, 1)
+    g = gold["gamma"]
+    want_o = gold["out"].reshape(1, 1, 3, 1)
+    want_s = gold["state"].reshape(1, 1, 1, 1)
+    res = _all_forms(o, q, k, v, g, chunks=(1, 2, 3, 4))
+    for name, (out, S) in res.items():
+        assert np.array_equal(out, want_o), (name, out.ravel(), want_o.ravel())
+        if S is not None:
+            assert np.array_equal(S, want_s), (name, S.ravel())
+
+
+def check_hand_expanded_vector(o):
+    gold = _read_golden("hand_expanded_vec.txt")
+    q = gold["q"].reshape(1, 1, 2, 2)
+    k = gold["k"].reshape(1, 1, 2, 2)
+    v = gold["v"].reshape(1, 1, 2, 2)
+    g = gold["gamma"]
+    want_o = gold["out_times_sqrt2"].reshape(1, 1, 2, 2) / math.sqrt(2.0)
+    want_s = gold["state"].reshape(1, 1, 2, 2)
+    res = _all_forms(o, q, k, v, g, chunks=(1, 2))
+    for name, (out, S) in res.items():
+        _close(out, want_o, 1e-15, name)
+        if S is not None:
+            assert np.array_equal(S, want_s), (name, S.ravel())
+
+
+def check_one_step_from_state(o):
+    """One recurrent step from a given state: S' = g S + k v, o = q S' (d = 1)."""
+    q = np.array([4.0]).reshape(1, 1, 1, 1)
+    k = np.array([3.0]).reshape(1, 1, 1, 1)
+    v = np.array([-1.0]).reshape(1, 1, 1, 1)
+    S0 = np.array([2.0]).reshape(1, 1, 1, 1)
+    out, S = o.recurrent(q, k, v, np.array([0.5]), state=S0)
+    assert S.ravel()[0] == 0.5 * 2.0 + 3.0 * -1.0      # -2
+    assert out.ravel()[0] == 4.0 * (0.5 * 2.0 - 3.0)   # -8
+    out_c, S_c = o.chunkwise(q, k, v, np.array([0.5]), 1, state_in=S0)
+    assert out_c.ravel()[0] == -8.0 and S_c.ravel()[0] == -2.0
+
+
+# --- closed forms ------------------------------------------------------------
+
+def check_closed_form_ones(o):
+    """q = k = 1 (length dk), v = 1: o_n = sqrt(dk) (1-g^(n+1))/(1-g), S = (1-g^N)/(1-g)."""
+    for dk, dv, N, g in ((4, 3, 37, 0.9), (9, 2, 20, 0.96875), (16, 5, 64, 0.5)):
+        q = np.ones((1, 1, N, dk))
+        k = np.ones((1, 1, N, dk))
+        v = np.ones((1, 1, N, dv))
+        n = np.arange(N, dtype=np.float64)
+        want = (math.sqrt(dk) * (1.0 - g ** (n + 1)) / (1.0 - g))[:, None] * np.ones(dv)
+        want_s = (1.0 - g ** N) / (1.0 - g) * np.ones((dk, dv))
+        res = _all_forms(o, q, k, v, np.array([g]), chunks=(1, 5, 16, N))
+        for name, (out, S) in res.items():
+            _close(out[0, 0], want, 1e-13, f"ones {name}")
+            if S is not None:
+                _close(S[0, 0], want_s, 1e-13, f"ones state {name}")
+        rows = o.parallel_rows(q[0, 0], k[0, 0], v[0, 0], g, [0, N // 2, N - 1])
+        _close(rows, want[[0, N // 2, N - 1]], 1e-13, "ones rows")
+
+
+def check_impulse(o):
+    """One non-zero key/value at m0: o_n = g^(n-m0) (q_n.k_m0/sqrt(dk)) v_m0, n >= m0; 0 before."""
+    N, dk, dv, m0, g = 24, 3, 4, 7, 0.8
+    q = _rand((1, 1, N, dk), 1)
+    k = np.zeros((1, 1, N, dk))
+    v = np.zeros((1, 1, N, dv))
+    k[0, 0, m0] = _rand(dk, 2)
+    v[0, 0, m0] = _rand(dv, 3)
+    want = np.zeros((N, dv))
+    for n in range(m0, N):
+        want[n] = g ** (n - m0) * (q[0, 0, n] @ k[0, 0, m0]) / math.sqrt(dk) * v[0, 0, m0]
+    want_s = g ** (N - 1 - m0) * np.outer(k[0, 0, m0], v[0, 0, m0])
+    res = _all_forms(o, q, k, v, np.array([g]), chunks=(1, 4, 5, N))
+    for name, (out, S) in res.items():
+        _close(out[0, 0], want, 1e-14, f"impulse {name}")
+        assert np.all(out[0, 0, :m0] == 0.0), f"impulse {name}: output before the impulse"
+        if S is not None:
+            _close(S[0, 0], want_s, 1e-14, f"impulse state {name}")
+    rows = o.parallel_rows(q[0, 0], k[0, 0], v[0, 0], g, [0, m0, N - 1])
+    _close(rows, want[[0, m0, N - 1]], 1e-14, "impulse rows")
+
+
+# --- special cases reducing to library routines --------------------------------
+
+def check_gamma_one_is_causal_linear_attention(o):
+    """gamma = 1: causal linear attention without normaliser, tril(QK^T)V/sqrt(dk)."""
+    B, H, N, dk, dv = 2, 2, 29, 6, 5
+    q, k, v = _rand((B, H, N, dk), 4), _rand((B, H, N, dk), 5), _rand((B, H, N, dv), 6)
+    want = np.tril(q @ np.swapaxes(k, -1, -2)) @ v / math.sqrt(dk)
+    want_s = np.swapaxes(k, -1, -2) @ v
+    res = _all_forms(o, q, k, v, np.ones(H), chunks=(1, 7, N))
+    for name, (out, S) in res.items():
+        _close(out, want, 1e-13, f"gamma=1 {name}")
+        if S is not None:
+            _close(S, want_s, 1e-13, f"gamma=1 state {name}")
+
+
+def check_gamma_zero_is_diagonal(o):
+    """gamma = 0: D = I, o_n = (q_n.k_n/sqrt(dk)) v_n and S = k_{N-1}^T v_{N-1}."""
+    B, H, N, dk, dv = 1, 2, 17, 4, 3
+    q, k, v = _rand((B, H, N, dk), 7), _rand((B, H, N, dk), 8), _rand((B, H, N, dv), 9)
+    want = np.sum(q * k, axis=-1, keepdims=True) / math.sqrt(dk) * v
+    want_s = k[:, :, -1, :, None] * v[:, :, -1, None, :]
+    res = _all_forms(o, q, k, v, np.zeros(H), chunks=(1, 4, N))
+    for name, (out, S) in res.items():
+        _close(out, want, 1e-14, f"gamma=0 {name}")
+        if S is not None:
+            _close(S, want_s, 1e-14, f"gamma=0 state {name}")
+
+
+# --- the pages' invariant and structural properties ---------------------------
+
+def check_three_forms_equal(o):
+    """Parallel == recurrent == chunkwise, for every chunk size, ragged tails included."""
+    B, H, dk, dv = 2, 3, 8, 6
+    g = o.gamma(np.arange(H))
+    for N in (1, 16, 45):
+        q, k, v = (_rand((B, H, N, dk), 10 + N), _rand((B, H, N, dk), 11 + N),
+                   _rand((B, H, N, dv), 12 + N))
+        res = _all_forms(o, q, k, v, g, chunks=(1, 2, 3, 7, 16, N, N + 5))
+        ref_out, ref_s = res["recurrent"]
+        for name, (out, S) in res.items():
+            _close(out, ref_out, 1e-12, f"N={N} {name} vs recurrent")
+            if S is not None:
+                _close(S, ref_s, 1e-12, f"N={N} {name} state vs recurrent")
+        for b, h in ((0, 0), (1, 2)):
+            rows = [0, N // 2, N - 1]
+            got = o.parallel_rows(q[b, h], k[b, h], v[b, h], g[h], rows)
+            _close(got, ref_out[b, h, rows], 1e-12, f"N={N} rows ({b},{h})")
+
+
+def check_linearity_and_heads(o):
+    """Output is linear in V and in Q; permuting heads with their gammas permutes outputs."""
+    B, H, N, dk, dv = 1, 4, 21, 5, 4
+    q, k = _rand((B, H, N, dk), 20), _rand((B, H, N, dk), 21)
+    v1, v2 = _rand((B, H, N, dv), 22), _rand((B, H, N, dv), 23)
+    g = np.array([0.9, 0.5, 0.99, 0.7])
+    o1, _ = o.chunkwise(q, k, v1, g, 4)
+    o2, _ = o.chunkwise(q, k, v2, g, 4)
+    o12, _ = o.chunkwise(q, k, 2.0 * v1 - 3.0 * v2, g, 4)
+    _close(o12, 2.0 * o1 - 3.0 * o2, 1e-13, "linear in V")
+    q2 = _rand((B, H, N, dk), 24)
+    oq, _ = o.chunkwise(q2, k, v1, g, 4)
+    oqq, _ = o.chunkwise(q + q2, k, v1, g, 4)
+    _close(oqq, o1 + oq, 1e-13, "linear in Q")
+    perm = np.array([2, 0, 3, 1])
+    op, Sp = o.chunkwise(q[:, perm], k[:, perm], v1[:, perm], g[perm], 4)
+    _, S1 = o.chunkwise(q, k, v1, g, 4)
+    _close(op, o1[:, perm], 1e-15, "head permutation")
+    _close(Sp, S1[:, perm], 1e-15, "head permutation state")
+
+
+def check_state_continuation(o):
+    """The state summarises the past: prefix state + recurrent/chunkwise on the rest == whole."""
+    B, H, N, dk, dv, cut = 1, 2, 40, 6, 7, 23
+    g = np.array([0.95, 0.8])
+    q, k, v = _rand((B, H, N, dk), 30), _rand((B, H, N, dk), 31), _rand((B, H, N, dv), 32)
+    full_o, full_s = o.chunkwise(q, k, v, g, 8)
+    pre_o, pre_s = o.chunkwise(q[:, :, :cut], k[:, :, :cut], v[:, :, :cut], g, 8)
+    rest_o, rest_s = o.recurrent(q[:, :, cut:], k[:, :, cut:], v[:, :, cut:], g, state=pre_s)
+    _close(pre_o, full_o[:, :, :cut], 1e-13, "prefix")
+    _close(rest_o, full_o[:, :, cut:], 1e-13, "continuation (recurrent)")
+    _close(rest_s, full_s, 1e-13, "continuation state (recurrent)")
+    rest_o2, rest_s2 = o.chunkwise(q[:, :, cut:], k[:, :, cut:], v[:, :, cut:], g, 5,
+                                   state_in=pre_s)
+    _close(rest_o2, full_o[:, :, cut:], 1e-13, "continuation (chunkwise)")
+    _close(rest_s2, full_s, 1e-13, "continuation state (chunkwise)")
+
+
+def check_empty_sequence(o):
+    """N = 0: no outputs; the final state is the starting state (zero by default)."""
+    q = np.zeros((1, 2, 0, 4))
+    v = np.zeros((1, 2, 0, 3))
+    out, S = o.chunkwise(q, q, v, np.array([0.9, 0.5]), 4)
+    assert out.shape == (1, 2, 0, 3) and np.all(S == 0.0)
+    S0 = _rand((1, 2, 4, 3), 40)
+    _, S2 = o.recurrent(q, q, v, np.array([0.9, 0.5]), state=S0)
+    assert np.array_equal(S2, S0)
+
+
+ALL_CHECKS = [
+    check_gamma_printed,
+    check_hand_expanded_scalar,
+    check_hand_expanded_vector,
+    check_one_step_from_state,
+    check_closed_form_ones,
+    check_impulse,
+    check_gamma_one_is_causal_linear_attention,
+    check_gamma_zero_is_diagonal,
+    check_three_forms_equal,
+    check_linearity_and_heads,
+    check_state_continuation,
+    check_empty_sequence,
+]
