@@ -1,0 +1,172 @@
+/*
+ * retention.h -- C ABI of libretention.so: RetNet multi-scale retention on
+ * one NVIDIA B300 (sm_103a).
+ *
+ * The operation (per batch row b and head h, 0-based positions n, m):
+ *
+ *   out[b,h,n,:] = sum_{m <= n} gamma_h^(n-m) * (q[b,h,n,:] . k[b,h,m,:]) / sqrt(dk) * v[b,h,m,:]
+ *
+ * i.e. O = ((Q K^T / sqrt(dk)) (.) D_h) V with the causal decay matrix
+ * D_h[n,m] = gamma_h^(n-m) for n >= m and 0 otherwise, and the recurrent state
+ *
+ *   S[b,h] = sum_m gamma_h^(N-1-m) k[b,h,m,:]^T v[b,h,m,:]      (dk x dv)
+ *
+ * Sources: "RetNet Guide: Retentive Networks & The Impossible Triangle",
+ * sections "3. Multi-Scale Retention (MSR)" (gamma_h = 1 - 2^(-5-h)),
+ * "1. The Parallel Representation ..." (D and R = ((QK^T) (.) D) V),
+ * "2. The Recurrent Representation ..." (S_n = gamma S_{n-1} + K_n^T V_n,
+ * R_n = Q_n S_n), "3. The Chunkwise Recurrent Representation ..." (chunk
+ * state carry and the zeta_j = gamma^(j+1) cross-chunk weight) and
+ * "1. PyTorch Implementation of MultiScaleRetention" (0-based heads, the
+ * 1/sqrt(d) scaling of the query).  The factor 1/sqrt(dk) multiplies the
+ * query only; states hold unscaled k^T v sums, so a state produced by
+ * retention_chunkwise can be advanced by retention_step.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All data pointers are DEVICE pointers on the current CUDA device, owned by
+ *   the caller, 16-byte aligned, dense and row-major:
+ *     q, k  [B][H][N][dk]       v, out  [B][H][N][dv]      (sequence calls)
+ *     q, k  [B][H][dk]          v, out  [B][H][dv]         (step calls)
+ *     state, state_out  [B][H][dk][dv]  float32
+ *     gamma  [H]  float32, each value in [0, 1]
+ * - Element type: the base names take bfloat16 q, k, v, out; the *_f32 names
+ *   take float32 q, k, v, out.  Accumulation is float32 everywhere.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *   asynchronous: they enqueue work on `stream` and never synchronise the
+ *   device.  Inputs must stay valid until that work has run.
+ * - out must not alias q, k or v.
+ * - Return value: RET_OK, or a negative ret_status.  Argument checks run on
+ *   the host before anything is enqueued; on a non-OK return nothing was
+ *   enqueued (except RET_ERR_CUDA, where a launch may have been attempted).
+ * - A device-side wait in the tensor-core kernels that exceeds its time
+ *   limit sets a bit in the library's device status word (see
+ *   retention_device_status) and the kernel returns; outputs are then
+ *   undefined.
+ */
+#ifndef RETENTION_H
+#define RETENTION_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RET_OK = 0,
+    RET_ERR_INVALID = -1,     /* null pointer, size < 0 (or 0 where not allowed), misaligned pointer */
+    RET_ERR_UNSUPPORTED = -2, /* valid arguments outside what the kernels handle (shape, chunk) */
+    RET_ERR_CUDA = -3         /* a CUDA runtime call or a kernel launch failed */
+} ret_status;
+
+/* Device status bits (retention_device_status). */
+#define RET_DEV_WAIT_TIMEOUT 0x1u /* a bounded barrier wait gave up */
+
+/*
+ * retention_chunkwise -- chunkwise recurrent forward, bf16 q/k/v/out.
+ *
+ * Per "3. The Chunkwise Recurrent Representation ...": the sequence is cut
+ * into chunks of `chunk` tokens; inside a chunk the parallel form runs on the
+ * tensor cores, and a float32 state S (dk x dv) is carried from chunk to
+ * chunk as S <- gamma^L S + sum_j gamma^(L-1-j) k_j^T v_j (L = chunk length;
+ * the last chunk may be shorter when N % chunk != 0).  The state starts at
+ * zero.  If state_out is not NULL it receives the state after token N-1
+ * (zero when N == 0).
+ *
+ * Supported: chunk in {64, 128}; dk in {128, 256}; dv a multiple of 64
+ * (at most 1024); N >= 0.  Other shapes return RET_ERR_UNSUPPORTED.  When the
+ * call splits the sequence into segments to fill the GPU it allocates a
+ * float32 scratch buffer stream-ordered (cudaMallocAsync / cudaFreeAsync on
+ * `stream`); retention_chunkwise_ws takes a caller-provided buffer instead.
+ */
+int retention_chunkwise(const void *q, const void *k, const void *v, const float *gamma,
+                        void *out, float *state_out,
+                        int B, int H, int N, int dk, int dv, int chunk, void *stream);
+
+/*
+ * retention_chunkwise_workspace_size -- bytes of scratch retention_chunkwise_ws
+ * needs for this shape (0 when the plan does not split the sequence).
+ * Host only; returns RET_ERR_INVALID / RET_ERR_UNSUPPORTED like
+ * retention_chunkwise would.
+ */
+int retention_chunkwise_workspace_size(int B, int H, int N, int dk, int dv, int chunk,
+                                       size_t *bytes);
+
+/*
+ * retention_chunkwise_ws -- retention_chunkwise with caller-owned scratch:
+ * `workspace` is a device buffer of at least `workspace_bytes` bytes (as given
+ * by retention_chunkwise_workspace_size; may be NULL when that is 0), 256-byte
+ * aligned, used only by the work this call enqueues.  No memory is allocated.
+ */
+int retention_chunkwise_ws(const void *q, const void *k, const void *v, const float *gamma,
+                           void *out, float *state_out,
+                           int B, int H, int N, int dk, int dv, int chunk,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * retention_chunkwise_launches -- number of kernels one retention_chunkwise
+ * call with these sizes enqueues (for launch accounting).  Host only.
+ */
+int retention_chunkwise_launches(int B, int H, int N, int dk, int dv, int chunk, int *launches);
+
+/*
+ * retention_chunkwise_f32 -- the chunkwise form with float32 q/k/v/out on the
+ * CUDA cores (plain fp32 FMA, no TF32).  chunk in [1, 128]; dk, dv in
+ * [1, 256]; the per-block working set must fit in shared memory, else
+ * RET_ERR_UNSUPPORTED.
+ */
+int retention_chunkwise_f32(const float *q, const float *k, const float *v, const float *gamma,
+                            float *out, float *state_out,
+                            int B, int H, int N, int dk, int dv, int chunk, void *stream);
+
+/*
+ * retention_parallel / retention_parallel_f32 -- the parallel form
+ * ("1. The Parallel Representation ..."): O = ((QK^T/sqrt(dk)) (.) D) V over
+ * the whole sequence, no state.  Exported for correctness checks; tiled on
+ * the CUDA cores.  dk, dv in [1, 256]; N >= 0.
+ */
+int retention_parallel(const void *q, const void *k, const void *v, const float *gamma,
+                       void *out, int B, int H, int N, int dk, int dv, void *stream);
+int retention_parallel_f32(const float *q, const float *k, const float *v, const float *gamma,
+                           float *out, int B, int H, int N, int dk, int dv, void *stream);
+
+/*
+ * retention_step / retention_step_f32 -- one recurrent decode step for every
+ * (b, h) ("2. The Recurrent Representation ..."):
+ *   S[b,h] <- gamma_h S[b,h] + k[b,h]^T v[b,h]     (in place, float32)
+ *   out[b,h] = (q[b,h] / sqrt(dk)) S[b,h]          (the updated state)
+ * There is no gamma argument: gamma_h = 1 - 2^(-5-h) for the 0-based head
+ * index h, rounded once to float32 (the values retention_gamma_schedule
+ * returns).  dv must be a multiple of 4; dk >= 1.
+ */
+int retention_step(const void *q, const void *k, const void *v, float *state, void *out,
+                   int B, int H, int dk, int dv, void *stream);
+int retention_step_f32(const float *q, const float *k, const float *v, float *state, float *out,
+                       int B, int H, int dk, int dv, void *stream);
+
+/*
+ * retention_gamma_schedule -- host function: gamma_out[h] = 1 - 2^(-5-h),
+ * h = 0..H-1, rounded to float32 ("3. Multi-Scale Retention (MSR)",
+ * 0-based heads).  gamma_out is HOST memory of H floats.
+ */
+int retention_gamma_schedule(int H, float *gamma_out);
+
+/*
+ * retention_device_status -- copies the library's device status word of the
+ * current device into *flags (RET_DEV_* bits; 0 = no fault seen) and clears
+ * it when `clear` is non-zero.  Synchronises the device.
+ */
+int retention_device_status(unsigned int *flags, int clear);
+
+/* retention_status_string -- static text for a ret_status value. */
+const char *retention_status_string(int status);
+
+/* retention_version -- ABI version (major * 100 + minor). */
+int retention_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RETENTION_H */

@@ -1,0 +1,236 @@
+"""ctypes binding of libretention.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/retention.h)
+and does nothing but check that the torch tensors it is given match what the
+C function expects (device, dtype, shape, contiguity), allocate the outputs
+the caller did not pass, and pass raw device pointers plus the current CUDA
+stream.  Every step of the computation runs in the library's CUDA kernels.
+If the library is missing the call raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libretention.so")
+_lock = threading.Lock()
+_lib = None
+
+RET_OK = 0
+RET_ERR_INVALID = -1
+RET_ERR_UNSUPPORTED = -2
+RET_ERR_CUDA = -3
+RET_DEV_WAIT_TIMEOUT = 0x1
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_fp = ctypes.POINTER(ctypes.c_float)
+
+# name -> argument types (all return int status unless noted)
+_SIGNATURES = {
+    "retention_chunkwise": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+    "retention_chunkwise_ws": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
+                               ctypes.c_size_t, _vp],
+    "retention_chunkwise_workspace_size": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)],
+    "retention_chunkwise_launches": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)],
+    "retention_chunkwise_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+    "retention_parallel": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "retention_parallel_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "retention_step": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
+    "retention_step_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
+    "retention_gamma_schedule": [_i, _fp],
+    "retention_device_status": [ctypes.POINTER(ctypes.c_uint), _i],
+    "retention_status_string": [_i],
+    "retention_version": [],
+}
+
+
+class RetentionError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: status {status} ({text})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RetentionError("load", RET_ERR_CUDA,
+                                     f"{LIB_PATH} is missing; build it with "
+                                     "linear_attention_sequence_02_b300.build.build()")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, args in _SIGNATURES.items():
+                fn = getattr(l, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_char_p if name == "retention_status_string" else ctypes.c_int
+            _lib = l
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != RET_OK:
+        raise RetentionError(fn, status, lib().retention_status_string(status).decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gamma_schedule(H: int) -> torch.Tensor:
+    """CPU float32 tensor [H]: gamma_h = 1 - 2^(-5-h) as the library computes it."""
+    out = (ctypes.c_float * H)()
+    _check("retention_gamma_schedule", lib().retention_gamma_schedule(H, out))
+    return torch.tensor(list(out), dtype=torch.float32)
+
+
+def device_status(clear: bool = True) -> int:
+    flags = ctypes.c_uint(0)
+    _check("retention_device_status", lib().retention_device_status(ctypes.byref(flags), int(clear)))
+    return int(flags.value)
+
+
+def _seq_dims(q, v):
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, H, N, dk = q.shape
+    return B, H, N, dk, v.shape[-1]
+
+
+def _sequence_call(fn, dtype, q, k, v, gamma, out, state_out, want_state, extra, stream):
+    B, H, N, dk, dv = _seq_dims(q, v)
+    _need(q, "q", dtype, (B, H, N, dk))
+    _need(k, "k", dtype, (B, H, N, dk))
+    _need(v, "v", dtype, (B, H, N, dv))
+    _need(gamma, "gamma", torch.float32, (H,))
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=dtype, device=q.device)
+    _need(out, "out", dtype, (B, H, N, dv))
+    if state_out is None and want_state:
+        state_out = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if state_out is not None:
+        _need(state_out, "state_out", torch.float32, (B, H, dk, dv))
+    args = [_p(q), _p(k), _p(v), _p(gamma), _p(out)]
+    if state_out is not None or fn.startswith("retention_chunkwise"):
+        args.append(_p(state_out))
+    args += [B, H, N, dk, dv, *extra]
+    return args, out, state_out
+
+
+def retention_chunkwise(q, k, v, gamma, chunk: int, out=None, state_out=None,
+                        want_state: bool = True, stream=None):
+    """bf16 chunkwise forward; returns (out, state_out or None)."""
+    args, out, state_out = _sequence_call("retention_chunkwise", torch.bfloat16, q, k, v, gamma,
+                                          out, state_out, want_state, [int(chunk)], stream)
+    _check("retention_chunkwise", lib().retention_chunkwise(*args, _stream(stream)))
+    return out, state_out
+
+
+def retention_chunkwise_ws(q, k, v, gamma, chunk: int, workspace, out=None, state_out=None,
+                           want_state: bool = True, stream=None):
+    """bf16 chunkwise forward with a caller-owned uint8 CUDA workspace tensor."""
+    args, out, state_out = _sequence_call("retention_chunkwise_ws", torch.bfloat16, q, k, v, gamma,
+                                          out, state_out, want_state, [int(chunk)], stream)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("retention_chunkwise_ws", lib().retention_chunkwise_ws(*args, ws_ptr, ws_bytes,
+                                                                  _stream(stream)))
+    return out, state_out
+
+
+def chunkwise_workspace_size(B, H, N, dk, dv, chunk) -> int:
+    n = ctypes.c_size_t(0)
+    _check("retention_chunkwise_workspace_size",
+           lib().retention_chunkwise_workspace_size(B, H, N, dk, dv, chunk, ctypes.byref(n)))
+    return int(n.value)
+
+
+def chunkwise_launches(B, H, N, dk, dv, chunk) -> int:
+    n = ctypes.c_int(0)
+    _check("retention_chunkwise_launches",
+           lib().retention_chunkwise_launches(B, H, N, dk, dv, chunk, ctypes.byref(n)))
+    return int(n.value)
+
+
+def retention_chunkwise_f32(q, k, v, gamma, chunk: int, out=None, state_out=None,
+                            want_state: bool = True, stream=None):
+    """fp32 chunkwise forward on the CUDA cores; returns (out, state_out or None)."""
+    args, out, state_out = _sequence_call("retention_chunkwise_f32", torch.float32, q, k, v, gamma,
+                                          out, state_out, want_state, [int(chunk)], stream)
+    _check("retention_chunkwise_f32", lib().retention_chunkwise_f32(*args, _stream(stream)))
+    return out, state_out
+
+
+def _parallel(fn, dtype, q, k, v, gamma, out, stream):
+    B, H, N, dk, dv = _seq_dims(q, v)
+    _need(q, "q", dtype, (B, H, N, dk))
+    _need(k, "k", dtype, (B, H, N, dk))
+    _need(v, "v", dtype, (B, H, N, dv))
+    _need(gamma, "gamma", torch.float32, (H,))
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=dtype, device=q.device)
+    _need(out, "out", dtype, (B, H, N, dv))
+    _check(fn, getattr(lib(), fn)(_p(q), _p(k), _p(v), _p(gamma), _p(out), B, H, N, dk, dv,
+                                  _stream(stream)))
+    return out
+
+
+def retention_parallel(q, k, v, gamma, out=None, stream=None):
+    """bf16 parallel form; returns out."""
+    return _parallel("retention_parallel", torch.bfloat16, q, k, v, gamma, out, stream)
+
+
+def retention_parallel_f32(q, k, v, gamma, out=None, stream=None):
+    """fp32 parallel form; returns out."""
+    return _parallel("retention_parallel_f32", torch.float32, q, k, v, gamma, out, stream)
+
+
+def _step(fn, dtype, q, k, v, state, out, stream):
+    if q.dim() != 3:
+        raise ValueError("q, k, v must be [B, H, d] for a step")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(q, "q", dtype, (B, H, dk))
+    _need(k, "k", dtype, (B, H, dk))
+    _need(v, "v", dtype, (B, H, dv))
+    _need(state, "state", torch.float32, (B, H, dk, dv))
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=dtype, device=q.device)
+    _need(out, "out", dtype, (B, H, dv))
+    _check(fn, getattr(lib(), fn)(_p(q), _p(k), _p(v), _p(state), _p(out), B, H, dk, dv,
+                                  _stream(stream)))
+    return out
+
+
+def retention_step(q, k, v, state, out=None, stream=None):
+    """One bf16 decode step; updates `state` in place and returns out."""
+    return _step("retention_step", torch.bfloat16, q, k, v, state, out, stream)
+
+
+def retention_step_f32(q, k, v, state, out=None, stream=None):
+    """One fp32 decode step; updates `state` in place and returns out."""
+    return _step("retention_step_f32", torch.float32, q, k, v, state, out, stream)

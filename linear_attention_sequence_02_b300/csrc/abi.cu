@@ -1,0 +1,219 @@
+// abi.cu -- the extern "C" entry points declared in include/retention.h:
+// argument validation (host only, before anything is enqueued), planning and
+// dispatch to the kernels in simt.cu and chunk_tc.cu.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "retention.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Common checks of a sequence call (chunkwise / parallel).  When N == 0 the
+// data pointers may be NULL (nothing is read or written).
+int check_sequence(const void* q, const void* k, const void* v, const float* gamma, const void* out,
+                   const void* state_out, int B, int H, int N, int dk, int dv) {
+  if (B <= 0 || H <= 0 || N < 0 || dk <= 0 || dv <= 0) return RET_ERR_INVALID;
+  if ((int64_t)B * H > INT32_MAX) return RET_ERR_INVALID;
+  if (N > 0) {
+    if (!q || !k || !v || !gamma || !out) return RET_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+      return RET_ERR_INVALID;
+    if (!aligned(gamma, 4)) return RET_ERR_INVALID;
+  }
+  if (state_out && !aligned(state_out, 16)) return RET_ERR_INVALID;
+  return RET_OK;
+}
+
+int check_step(const void* q, const void* k, const void* v, const float* state, const void* out,
+               int B, int H, int dk, int dv) {
+  if (B <= 0 || H <= 0 || dk <= 0 || dv <= 0) return RET_ERR_INVALID;
+  if ((int64_t)B * H > INT32_MAX) return RET_ERR_INVALID;
+  if (!q || !k || !v || !state || !out) return RET_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(state, 16) ||
+      !aligned(out, 16))
+    return RET_ERR_INVALID;
+  if (dv % 4 != 0) return RET_ERR_UNSUPPORTED;
+  return RET_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? RET_OK : RET_ERR_CUDA; }
+
+// Zero the state of an empty sequence (the sum over no tokens).
+int zero_state(float* state_out, int B, int H, int dk, int dv, cudaStream_t s) {
+  if (!state_out) return RET_OK;
+  return from_cuda(cudaMemsetAsync(state_out, 0, sizeof(float) * (size_t)B * H * dk * dv, s));
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// The bf16 chunkwise plan for these sizes, or an error status.
+int plan_chunkwise(int B, int H, int N, int dk, int dv, int chunk, int sms, ret::ChunkPlan* plan) {
+  if (B <= 0 || H <= 0 || N < 0 || dk <= 0 || dv <= 0 || chunk <= 0) return RET_ERR_INVALID;
+  if (!ret::chunk_tc_plan(B, H, N, dk, dv, chunk, sms, plan)) return RET_ERR_UNSUPPORTED;
+  return RET_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int retention_version(void) { return 100; }
+
+const char* retention_status_string(int status) {
+  switch (status) {
+    case RET_OK: return "ok";
+    case RET_ERR_INVALID: return "invalid argument";
+    case RET_ERR_UNSUPPORTED: return "unsupported shape or chunk size";
+    case RET_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int retention_gamma_schedule(int H, float* gamma_out) {
+  if (H <= 0 || !gamma_out) return RET_ERR_INVALID;
+  for (int h = 0; h < H; ++h) {
+    // 1 - 2^(-5-h) rounded once to fp32 ("3. Multi-Scale Retention (MSR)", 0-based h);
+    // beyond h = 60 the double value is already 1 - tiny and rounds to 1.0f.
+    const double g = h > 60 ? 1.0 : 1.0 - ldexp(1.0, -5 - h);
+    gamma_out[h] = (float)g;
+  }
+  return RET_OK;
+}
+
+int retention_device_status(unsigned int* flags, int clear) {
+  if (!flags) return RET_ERR_INVALID;
+  return from_cuda(ret::read_device_status(flags, clear));
+}
+
+int retention_chunkwise_workspace_size(int B, int H, int N, int dk, int dv, int chunk,
+                                       size_t* bytes) {
+  if (!bytes) return RET_ERR_INVALID;
+  ret::ChunkPlan plan;
+  const int sms = num_sms();
+  int st = plan_chunkwise(B, H, N, dk, dv, chunk, sms > 0 ? sms : 148, &plan);
+  if (st != RET_OK) return st;
+  *bytes = plan.workspace_bytes;
+  return RET_OK;
+}
+
+int retention_chunkwise_launches(int B, int H, int N, int dk, int dv, int chunk, int* launches) {
+  if (!launches) return RET_ERR_INVALID;
+  ret::ChunkPlan plan;
+  const int sms = num_sms();
+  int st = plan_chunkwise(B, H, N, dk, dv, chunk, sms > 0 ? sms : 148, &plan);
+  if (st != RET_OK) return st;
+  *launches = N == 0 ? 0 : plan.launches;
+  return RET_OK;
+}
+
+int retention_chunkwise_ws(const void* q, const void* k, const void* v, const float* gamma,
+                           void* out, float* state_out, int B, int H, int N, int dk, int dv,
+                           int chunk, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  ret::ChunkPlan plan;
+  const int sms = num_sms();
+  if (sms <= 0) return RET_ERR_CUDA;
+  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
+  if (st != RET_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) return zero_state(state_out, B, H, dk, dv, s);
+  if (plan.workspace_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256))
+      return RET_ERR_INVALID;
+  }
+  return from_cuda(ret::launch_chunk_tc(q, k, v, gamma, out, state_out, B, H, N, dk, dv, chunk,
+                                        plan, static_cast<float*>(workspace), s));
+}
+
+int retention_chunkwise(const void* q, const void* k, const void* v, const float* gamma, void* out,
+                        float* state_out, int B, int H, int N, int dk, int dv, int chunk,
+                        void* stream) {
+  int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  ret::ChunkPlan plan;
+  const int sms = num_sms();
+  if (sms <= 0) return RET_ERR_CUDA;
+  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
+  if (st != RET_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) return zero_state(state_out, B, H, dk, dv, s);
+  float* ws = nullptr;
+  if (plan.workspace_bytes > 0) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), plan.workspace_bytes, s) != cudaSuccess)
+      return RET_ERR_CUDA;
+  }
+  cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, out, state_out, B, H, N, dk, dv, chunk,
+                                       plan, ws, s);
+  if (ws) {
+    cudaError_t e2 = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return from_cuda(e);
+}
+
+int retention_chunkwise_f32(const float* q, const float* k, const float* v, const float* gamma,
+                            float* out, float* state_out, int B, int H, int N, int dk, int dv,
+                            int chunk, void* stream) {
+  int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  if (chunk <= 0) return RET_ERR_INVALID;
+  if (chunk > 128 || dk > 256 || dv > 256) return RET_ERR_UNSUPPORTED;
+  if (ret::chunkwise_f32_smem_bytes(dk, chunk) > (size_t)ret::kMaxSmemPerBlock)
+    return RET_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return from_cuda(ret::launch_chunkwise_f32(q, k, v, gamma, out, state_out, B, H, N, dk, dv,
+                                             chunk, s));
+}
+
+int retention_parallel(const void* q, const void* k, const void* v, const float* gamma, void* out,
+                       int B, int H, int N, int dk, int dv, void* stream) {
+  int st = check_sequence(q, k, v, gamma, out, nullptr, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  if (dk > 256 || dv > 256) return RET_ERR_UNSUPPORTED;
+  if (N == 0) return RET_OK;
+  if (B * H > 65535) return RET_ERR_UNSUPPORTED;
+  return from_cuda(ret::launch_parallel_bf16(q, k, v, gamma, out, B, H, N, dk, dv,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int retention_parallel_f32(const float* q, const float* k, const float* v, const float* gamma,
+                           float* out, int B, int H, int N, int dk, int dv, void* stream) {
+  int st = check_sequence(q, k, v, gamma, out, nullptr, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  if (dk > 256 || dv > 256) return RET_ERR_UNSUPPORTED;
+  if (N == 0) return RET_OK;
+  if (B * H > 65535) return RET_ERR_UNSUPPORTED;
+  return from_cuda(ret::launch_parallel_f32(q, k, v, gamma, out, B, H, N, dk, dv,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int retention_step(const void* q, const void* k, const void* v, float* state, void* out, int B,
+                   int H, int dk, int dv, void* stream) {
+  int st = check_step(q, k, v, state, out, B, H, dk, dv);
+  if (st != RET_OK) return st;
+  if (dv > 4 * 65535 * 32) return RET_ERR_UNSUPPORTED;
+  return from_cuda(ret::launch_step_bf16(q, k, v, state, out, B, H, dk, dv,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int retention_step_f32(const float* q, const float* k, const float* v, float* state, float* out,
+                       int B, int H, int dk, int dv, void* stream) {
+  int st = check_step(q, k, v, state, out, B, H, dk, dv);
+  if (st != RET_OK) return st;
+  if (dv > 4 * 65535 * 32) return RET_ERR_UNSUPPORTED;
+  return from_cuda(ret::launch_step_f32(q, k, v, state, out, B, H, dk, dv,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

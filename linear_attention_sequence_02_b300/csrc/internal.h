@@ -1,0 +1,48 @@
+// internal.h -- declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/retention.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace ret {
+
+// Largest dynamic shared memory a block may opt into on sm_100-class parts.
+constexpr int kMaxSmemPerBlock = 232448;  // 227 KB
+
+// ---- SIMT kernels (simt.cu) -------------------------------------------------
+// Each returns a cudaError_t from the launch (cudaGetLastError after it).
+cudaError_t launch_step_bf16(const void* q, const void* k, const void* v, float* state, void* out,
+                             int B, int H, int dk, int dv, cudaStream_t s);
+cudaError_t launch_step_f32(const float* q, const float* k, const float* v, float* state,
+                            float* out, int B, int H, int dk, int dv, cudaStream_t s);
+cudaError_t launch_parallel_bf16(const void* q, const void* k, const void* v, const float* gamma,
+                                 void* out, int B, int H, int N, int dk, int dv, cudaStream_t s);
+cudaError_t launch_parallel_f32(const float* q, const float* k, const float* v,
+                                const float* gamma, float* out, int B, int H, int N, int dk,
+                                int dv, cudaStream_t s);
+// Shared memory bytes the fp32 chunkwise kernel needs (0 if dims are invalid).
+size_t chunkwise_f32_smem_bytes(int dk, int chunk);
+cudaError_t launch_chunkwise_f32(const float* q, const float* k, const float* v,
+                                 const float* gamma, float* out, float* state_out, int B, int H,
+                                 int N, int dk, int dv, int chunk, cudaStream_t s);
+
+// ---- tensor-core chunkwise (chunk_tc.cu) --------------------------------------
+struct ChunkPlan {
+  int dvt;          // value columns per CTA (64 or 128)
+  int n_dv_tiles;   // dv / dvt
+  int segments;     // sequence segments per head (>= 1)
+  int seg_chunks;   // chunks per segment (all segments but the last are full)
+  int n_chunks;     // ceil(N / chunk)
+  size_t workspace_bytes;  // float32 segment states, 0 if segments == 1
+  int launches;     // kernels enqueued by one call
+};
+// Fills `plan` for a supported shape; returns false for unsupported shapes.
+bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan);
+cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
+                            void* out, float* state_out, int B, int H, int N, int dk, int dv,
+                            int chunk, const ChunkPlan& plan, float* workspace, cudaStream_t s);
+cudaError_t read_device_status(unsigned int* flags, int clear);
+
+}  // namespace ret

@@ -1,0 +1,86 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+symbol include/retention.h declares; host-side validation rejects bad
+arguments before touching the device; the decay schedule is 1 - 2^(-5-h)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from linear_attention_sequence_02_b300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "retention.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(retention_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for must in ("retention_chunkwise", "retention_parallel", "retention_step",
+                 "retention_chunkwise_f32", "retention_parallel_f32", "retention_step_f32"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_symbols()) <= set(binding._SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.retention_version() >= 100
+    for st in (0, -1, -2, -3):
+        assert lib.retention_status_string(st)
+
+
+def test_gamma_schedule_matches_oracle(lib, orc):
+    H = 24
+    g = binding.gamma_schedule(H).numpy()
+    want = np.array([orc.gamma(h) for h in range(H)], dtype=np.float64).astype(np.float32)
+    assert np.array_equal(g, want)
+    # exact in fp32 up to h = 19: the schedule is the formula, not an approximation
+    assert np.array_equal(g[:20].astype(np.float64), orc.gamma(np.arange(20)))
+
+
+P = ctypes.c_void_p(0x1000)       # 16-byte aligned dummy device address (never dereferenced)
+P_ODD = ctypes.c_void_p(0x1004)   # misaligned dummy
+
+
+@pytest.mark.parametrize("args, want", [
+    ((None, P, P, P, P, None, 1, 1, 8, 128, 128, 64), binding.RET_ERR_INVALID),   # null q
+    ((P, P, P, P, P, None, 0, 1, 8, 128, 128, 64), binding.RET_ERR_INVALID),      # B = 0
+    ((P, P, P, P, P, None, 1, -1, 8, 128, 128, 64), binding.RET_ERR_INVALID),     # H < 0
+    ((P, P, P, P, P, None, 1, 1, -2, 128, 128, 64), binding.RET_ERR_INVALID),     # N < 0
+    ((P, P, P, P, P, None, 1, 1, 8, 0, 128, 64), binding.RET_ERR_INVALID),        # dk = 0
+    ((P_ODD, P, P, P, P, None, 1, 1, 8, 128, 128, 64), binding.RET_ERR_INVALID),  # misaligned q
+    ((P, P, P, P, P_ODD, None, 1, 1, 8, 128, 128, 64), binding.RET_ERR_INVALID),  # misaligned out
+    ((P, P, P, P, P, P_ODD, 1, 1, 8, 128, 128, 64), binding.RET_ERR_INVALID),     # misaligned state
+])
+def test_chunkwise_rejects_bad_arguments_on_host(lib, args, want):
+    assert lib.retention_chunkwise(*args, None) == want
+    assert lib.retention_chunkwise_ws(*args, None, 0, None) == want
+
+
+def test_f32_and_parallel_and_step_validation(lib):
+    assert lib.retention_chunkwise_f32(P, P, P, P, P, None, 1, 1, 8, 32, 32, 0, None) == binding.RET_ERR_INVALID
+    assert lib.retention_chunkwise_f32(P, P, P, P, P, None, 1, 1, 8, 32, 32, 129, None) == binding.RET_ERR_UNSUPPORTED
+    assert lib.retention_chunkwise_f32(P, P, P, P, P, None, 1, 1, 8, 300, 32, 32, None) == binding.RET_ERR_UNSUPPORTED
+    assert lib.retention_parallel(None, P, P, P, P, 1, 1, 8, 32, 32, None) == binding.RET_ERR_INVALID
+    assert lib.retention_parallel_f32(P, P, P, P, P, 1, 1, 8, 32, 512, None) == binding.RET_ERR_UNSUPPORTED
+    assert lib.retention_step(P, P, P, None, P, 1, 1, 32, 32, None) == binding.RET_ERR_INVALID
+    assert lib.retention_step(P, P, P, P, P, 1, 1, 32, 30, None) == binding.RET_ERR_UNSUPPORTED
+    assert lib.retention_step_f32(P, P, P, P, P_ODD, 1, 1, 32, 32, None) == binding.RET_ERR_INVALID
+    assert lib.retention_gamma_schedule(0, None) == binding.RET_ERR_INVALID
+    assert lib.retention_device_status(None, 0) == binding.RET_ERR_INVALID
