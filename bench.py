@@ -1,0 +1,466 @@
+"""Benchmark of the retention hot path on B300.
+
+Headline: chunkwise-forward tokens/s (B*N sequence positions per second, all
+heads included) on the mid workload B=4, H=8, N=2048, d_k=d_v=128, chunk=64,
+bf16 q/k/v/out with fp32 accumulation and state.  One step = one
+retention_chunkwise call over one batch; inputs are resident in HBM and L2 is
+flushed (a 512 MiB write) between timed steps, outside the timed events.
+
+Also reported on the same line:
+  decode      the recurrent decode step on 64 sequences x 16 heads, d_k=128,
+              d_v=256, fp32 state (128 MiB > L2): 1024 sequential steps
+              captured in one CUDA graph; steps/s and HBM roofline.
+  workloads   the long-context (B=1,H=16,N=16384,d_k=128,d_v=256,C=128) and
+              7B-shaped (B=8,H=16,N=8192,d_k=256,d_v=512,C=128) chunkwise runs.
+  e2e         the headline metric through host buffers: pinned host q/k/v
+              copied in, the call, out and state copied back, per step.
+  roofline    algorithmic bytes of one retention_chunkwise call (Q,K,V read,
+              out and final state written) over its CUDA-event duration,
+              against the measured HBM copy bandwidth.
+  cpu_baseline  the fp64 CPU oracle (chunkwise form, same chunk) on the host
+              cores, timed on the full mid workload.
+
+`--impl reference` times the fp64 CPU oracle alone on the same workload and
+metric (the full mid workload per step) and prints its own line.
+`--only {mid,long,7b,decode}` runs one workload alone and prints its timing
+(used to give ncu a small, single-workload command).
+Under torchrun each rank runs its own replica (independent batches, no
+collective on the data path); value = all ranks' tokens / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MID = dict(name="mid", B=4, H=8, N=2048, dk=128, dv=128, chunk=64)
+LONG = dict(name="long", B=1, H=16, N=16384, dk=128, dv=256, chunk=128)
+B7 = dict(name="7b", B=8, H=16, N=8192, dk=256, dv=512, chunk=128)
+DECODE = dict(name="decode", T=1024, B=64, H=16, dk=128, dv=256)
+METRIC = "retention tokens/s (chunkwise fwd, 1 B300) + decode steps/s; % of roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def chunk_bytes(w) -> int:
+    """Algorithmic HBM bytes of one chunkwise call: Q,K,V read, out written (bf16), S written (fp32)."""
+    B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
+    return B * H * N * (2 * dk + dv) * 2 + B * H * N * dv * 2 + B * H * dk * dv * 4
+
+
+def chunk_flops(w) -> int:
+    """Algorithmic flops of one chunkwise call (causal part only)."""
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    return B * H * N * ((dk + dv) * (C + 1) + 4 * dk * dv)
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic HBM bytes of one decode step: S read+write (fp32), q,k,v read, out written (bf16)."""
+    B, H, dk, dv = w["B"], w["H"], w["dk"], w["dv"]
+    return B * H * (8 * dk * dv + 2 * (2 * dk + dv) + 2 * dv)
+
+
+def kernel_sha() -> str:
+    path = os.path.join(ROOT, "linear_attention_sequence_02_b300", "csrc", "chunk_tc.cu")
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per call from the committed ncu summary, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_sha()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == sha and parts[1] == workload:
+                return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[2:6]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def time_chunkwise(w, steps, warmup, dev, flush, seed=0):
+    """Per-call CUDA-event times (ms) of retention_chunkwise, L2 flushed between calls."""
+    from linear_attention_sequence_02_b300 import binding, inputs
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    q, k, v = (x.to(dev) for x in inputs.qkv(B, H, N, dk, dv, seed, torch.bfloat16))
+    g = binding.gamma_schedule(H).to(dev)
+    out = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
+    st = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush.zero_()
+        binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
+    torch.cuda.synchronize(dev)
+    times = []
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    times = [a.elapsed_time(b) for a, b in evs]
+    launches = binding.chunkwise_launches(B, H, N, dk, dv, C) * steps
+    del q, k, v, out, st
+    return times, launches
+
+
+def time_e2e(w, steps, warmup, dev, seed=0):
+    """Headline metric through host buffers: H2D of q,k,v, the call, D2H of out and state."""
+    from linear_attention_sequence_02_b300 import binding, inputs
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    qh, kh, vh = (x.pin_memory() for x in inputs.qkv(B, H, N, dk, dv, seed, torch.bfloat16))
+    oh = torch.empty(B, H, N, dv, dtype=torch.bfloat16).pin_memory()
+    sh = torch.empty(B, H, dk, dv, dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty_like(x, device=dev) for x in (qh, kh, vh))
+    od = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
+    sd = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    g = binding.gamma_schedule(H).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        binding.retention_chunkwise(qd, kd, vd, g, C, out=od, state_out=sd)
+        oh.copy_(od, non_blocking=True)
+        sh.copy_(sd, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + sh.numel() * sh.element_size()
+    return ms, h2d, d2h
+
+
+def time_decode(w, reps, dev, seed=0):
+    """ms per step of 1024 retention_step launches captured in one CUDA graph."""
+    from linear_attention_sequence_02_b300 import binding, inputs
+    T, B, H, dk, dv = w["T"], w["B"], w["H"], w["dk"], w["dv"]
+    q, k, v = (x.to(dev) for x in inputs.decode_steps(T, B, H, dk, dv, seed))
+    state = inputs.decode_state(B, H, dk, dv, seed).to(dev)
+    outs = torch.empty(T, B, H, dv, dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for t in range(3):  # warm-up outside capture
+            binding.retention_step(q[t], k[t], v[t], state, out=outs[t], stream=side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream(dev)
+        for t in range(T):
+            binding.retention_step(q[t], k[t], v[t], state, out=outs[t], stream=cap)
+    stream = torch.cuda.current_stream(dev)
+    graph.replay()  # warm-up replay
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b) / T)
+    del graph, q, k, v, outs, state
+    return times
+
+
+def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
+    """fp64 oracle (chunkwise form, same chunk) on the full workload, repeated for >= min_seconds."""
+    import oracle
+    from linear_attention_sequence_02_b300 import binding, inputs
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    q, k, v = inputs.qkv(B, H, N, dk, dv, 0, torch.bfloat16)
+    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    g = binding.gamma_schedule(H).double().numpy()
+    orc = oracle.default()
+    passes, t0 = 0, time.perf_counter()
+    while passes < max_passes and (time.perf_counter() - t0) < min_seconds:
+        orc.chunkwise(qd, kd, vd, g, C)
+        passes += 1
+    dt = (time.perf_counter() - t0) / passes
+    return {"value": round(B * N / dt, 1), "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": f"full {w['name']} workload (B={B},H={H},N={N},dk={dk},dv={dv},chunk={C}), "
+                      f"{passes} fp64 passes, {dt:.3f} s each"}
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from linear_attention_sequence_02_b300 import binding
+    binding.lib()
+    hbm, tflops, peak_kind = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # ---- headline: mid chunkwise, device-timed ----
+    w = MID
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        times, launches = time_chunkwise(w, args.steps, args.warmup, dev, flush)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = max_over_ranks(sum(times), world, dev)
+    ms = total_ms / args.steps
+    tokens = w["B"] * w["N"] * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    avg_s = sum(times) / len(times) / 1e3
+    achieved = chunk_bytes(w) / avg_s / 1e9
+    traffic = recorded_traffic(w["name"])
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "peak_kind": peak_kind, "kernel": "retention_chunkwise call (pre-pass + main)",
+                "algorithmic_bytes_per_call": chunk_bytes(w),
+                "tensor_flops_frac": round(chunk_flops(w) / avg_s / 1e12 / tflops, 4)}
+
+    # ---- e2e through host buffers ----
+    e2e_ms, h2d, d2h = time_e2e(w, max(3, args.steps // 2), max(3, args.warmup), dev)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e = {"value": round(w["B"] * w["N"] * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    extra = {}
+    # ---- decode step ----
+    if not args.quick:
+        dt = time_decode(DECODE, 3, dev)
+        step_ms = statistics.median(dt)
+        bytes_step = decode_bytes(DECODE)
+        extra["decode"] = {
+            "steps_per_s": round(1e3 / step_ms, 1),
+            "tokens_per_s": round(DECODE["B"] * 1e3 / step_ms, 1),
+            "ms_per_step": round(step_ms, 5),
+            "config": {"batch": DECODE["B"], "H": DECODE["H"], "dk": DECODE["dk"], "dv": DECODE["dv"],
+                       "steps": DECODE["T"], "graph": "1024 launches in one CUDA graph",
+                       "l2": "fp32 state 128 MiB > L2"},
+            "roofline": {"bound": "hbm", "achieved": round(bytes_step / (step_ms / 1e3) / 1e9, 1),
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": round(bytes_step / (step_ms / 1e3) / 1e9 / hbm, 4),
+                         "traffic": recorded_traffic("decode_step")},
+            "gpu_launches": DECODE["T"] * 3,
+        }
+        for wl in (LONG, B7):
+            t, n = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
+            a_s = statistics.median(t) / 1e3
+            ach = chunk_bytes(wl) / a_s / 1e9
+            extra[wl["name"]] = {
+                "tokens_per_s": round(wl["B"] * wl["N"] / a_s, 1), "ms_per_call": round(a_s * 1e3, 4),
+                "config": {k: wl[k] for k in ("B", "H", "N", "dk", "dv", "chunk")},
+                "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(ach / hbm, 4), "traffic": recorded_traffic(wl["name"]),
+                             "tensor_flops_frac": round(chunk_flops(wl) / a_s / 1e12 / tflops, 4)},
+                "gpu_launches": n}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1) q,k,v)",
+        "config": {"workload": "mid retention chunkwise fwd", "B": w["B"], "H": w["H"], "N": w["N"],
+                   "dk": w["dk"], "dv": w["dv"], "chunk": w["chunk"], "global_batch": w["B"] * world,
+                   "seq_len": w["N"], "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "flushed (512 MiB write) between timed steps"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    line.update(extra)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_chunkwise(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from linear_attention_sequence_02_b300 import inputs
+    w = MID
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    q, k, v = inputs.qkv(B, H, N, dk, dv, 0, torch.bfloat16)
+    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    g = [oracle.gamma(h) for h in range(H)]
+    orc = oracle.default()
+    for _ in range(args.warmup):
+        orc.chunkwise(qd, kd, vd, g, C)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.chunkwise(qd, kd, vd, g, C)
+    full_s = (time.perf_counter() - t0) / args.steps
+    value = B * N / full_s
+    sample = f"full mid workload per step (all {B * H} heads), fp64 chunkwise form, chunk {C}"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(full_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded iid N(0,1) q,k,v)",
+            "config": {"workload": "mid retention chunkwise fwd", "B": B, "H": H, "N": N, "dk": dk,
+                       "dv": dv, "chunk": C, "global_batch": B, "seq_len": N,
+                       "parallelism": "host cores (OpenMP over heads)"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": orc.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_only(args):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    if args.only == "decode":
+        t = time_decode(DECODE, args.steps, dev)
+        print(json.dumps({"only": "decode", "ms_per_step": statistics.median(t)}))
+        return
+    w = {"mid": MID, "long": LONG, "7b": B7}[args.only]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    t, n = time_chunkwise(w, args.steps, args.warmup, dev, flush)
+    print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": n}))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["mid", "long", "7b", "decode"], default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.only:
+        run_only(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
