@@ -105,6 +105,33 @@ int retention_chunkwise_ws(const void *q, const void *k, const void *v, const fl
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * retention_chunkwise_noalloc -- retention_chunkwise for callers that must not
+ * allocate device memory.  The paper has no counterpart to this entry point;
+ * it exists for callers such as serving runtimes that plan all device memory
+ * at start-up under a fixed budget (an allocation on the request path can
+ * fail, stall or fragment the pool) and embedders whose host code may not call
+ * the CUDA allocator.  Same arguments, layout and results as
+ * retention_chunkwise; it allocates and frees nothing.
+ *
+ * Scratch: the segment states live in a file-scope device array of
+ * 8 MiB (8388608 bytes) that every GPU loading the library reserves until the
+ * process exits.  Shapes whose plan needs more scratch than that (see
+ * retention_chunkwise_workspace_size) return RET_ERR_UNSUPPORTED before
+ * anything is enqueued.  Nothing in the array has to start at zero: each call
+ * writes every slot it later reads, so stale contents of an earlier call are
+ * never used.
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) once; make that first call
+ * before any stream capture.
+ * Concurrency: every call on a device shares the one array, so calls whose
+ * work overlaps on the GPU (different streams, or different host threads
+ * without ordering) race on it; order them on one stream or serialise them.
+ */
+int retention_chunkwise_noalloc(const void *q, const void *k, const void *v, const float *gamma,
+                                void *out, float *state_out,
+                                int B, int H, int N, int dk, int dv, int chunk, void *stream);
+
+/*
  * retention_chunkwise_launches -- number of kernels one retention_chunkwise
  * call with these sizes enqueues (for launch accounting).  Host only.
  */

@@ -35,6 +35,7 @@ _SIGNATURES = {
     "retention_chunkwise": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_chunkwise_ws": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                ctypes.c_size_t, _vp],
+    "retention_chunkwise_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_chunkwise_workspace_size": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)],
     "retention_chunkwise_launches": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)],
     "retention_chunkwise_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
@@ -159,6 +160,16 @@ def retention_chunkwise_ws(q, k, v, gamma, chunk: int, workspace, out=None, stat
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("retention_chunkwise_ws", lib().retention_chunkwise_ws(*args, ws_ptr, ws_bytes,
                                                                   _stream(stream)))
+    return out, state_out
+
+
+def retention_chunkwise_noalloc(q, k, v, gamma, chunk: int, out=None, state_out=None,
+                                want_state: bool = True, stream=None):
+    """bf16 chunkwise forward that allocates nothing: the library's static
+    device scratch holds the segment states (callers allocate out/state_out)."""
+    args, out, state_out = _sequence_call("retention_chunkwise_noalloc", torch.bfloat16, q, k, v,
+                                          gamma, out, state_out, want_state, [int(chunk)], stream)
+    _check("retention_chunkwise_noalloc", lib().retention_chunkwise_noalloc(*args, _stream(stream)))
     return out, state_out
 
 
