@@ -1,37 +1,64 @@
 // chunk_tc.cu -- chunkwise retention forward on the sm_103a tensor cores.
 //
-// Per head (b, h) and 64- or 128-wide slab of value columns, for each chunk of
-// C tokens (section "3. The Chunkwise Recurrent Representation ..." of "RetNet
-// Guide: Retentive Networks & The Impossible Triangle"; the in-chunk decay of
-// the state update is the reading that makes the chunkwise form equal the
-// recurrent one):
+// One CTA handles one (head b*H+h, 64- or 128-wide slab of value columns,
+// run of consecutive chunks).  For chunk i (tokens t, m = 0..L-1 inside the
+// chunk, L = C except for a ragged last chunk) section "3. The Chunkwise
+// Recurrent Representation ..." of "RetNet Guide: Retentive Networks & The
+// Impossible Triangle" gives, with the in-chunk decay of the state update made
+// explicit (the reading under which the chunkwise form equals the recurrent
+// one):
 //
-//   P   = Q_i K_i^T                          (tcgen05, fp32 in TMEM)
-//   P~  = (P (.) D_C) / sqrt(dk) -> bf16     (registers; D_C[r][c] = gamma^(r-c), r >= c)
-//   W   = diag(gamma^(L-1-j)) V_i -> bf16    (shared memory)
-//   O1  = Q_i S_{i-1}                        (tcgen05; S_{i-1} copied to bf16)
-//   O2  = P~ V_i                             (tcgen05)
-//   out = O2 + diag(gamma^(j+1)) O1 / sqrt(dk)   (registers -> bf16 -> TMA store)
-//   S_i = gamma^L S_{i-1} + K_i^T W          (fp32 state kept in TMEM across chunks)
+//   out_t = scale [ sum_{m<=t} gamma^(t-m) (q_t . k_m) v_m + gamma^(t+1) q_t S_{i-1} ]
+//   S_i   = gamma^L S_{i-1} + sum_m gamma^(L-1-m) k_m^T v_m          (scale = 1/sqrt(dk))
 //
-// Roles inside a CTA of 192 threads:
-//   warp 0 lane 0 : TMA producer (Q, K, V boxes into an NS-deep stage ring)
+// Rescaled form (heads with gamma^C >= 2^-14, which includes every head of the
+// schedule gamma_h = 1 - 2^(-5-h)).  The tensor memory holds S^ = c S with a
+// running factor c in [1, 2).  Per chunk, n = floor(log2(c / gamma^L)) and
+// c' = 2^-n c / gamma^L, and with w_m = c' gamma^(L-1-m) and W = diag(w) V:
+//
+//   S^_i = 2^-n S^_{i-1} + K^T W                  one MMA chain; 2^-n is the MMA's
+//                                                 accumulator scale operand
+//   O'   = tril(Q K^T) W + Q (2^-n S^_{i-1})      one accumulator, causal mask only
+//   out_t = O'_t * scale / (c' gamma^(L-1-t))
+//
+// (substituting w and c' gives back the two lines above exactly).  Every
+// factor lies in [gamma^(C-1), 2], so nothing overflows, and no pass over the
+// state in tensor memory sits on the chunk-to-chunk chain.
+//
+// Direct form (any other gamma in [0, 1]): the state is decayed explicitly in
+// tensor memory each chunk, P~ = (Q K^T (.) D) scale with D[t][m] = gamma^(t-m),
+// and, in place in shared memory after the Q K^T product has read them,
+// K <- diag(gamma^(L-1-m)) K and Q <- diag(scale gamma^(t+1)) Q, so that
+//   S_i = gamma^L S_{i-1} + K^T V,   out = P~ V + Q S_{i-1}.
+//
+// Roles in a CTA of 320 threads:
+//   warp 0 lane 0 : TMA producer: V tiles and 128-column halves of Q and K into
+//                   two shared-memory rings
 //   warp 1        : owns the TMEM allocation; lane 0 issues every tcgen05.mma
-//   warps 2..5    : epilogue; warp w reads TMEM lanes 32*(w%4) .. +31
+//   warps 2..5    : state group: W = diag(w) V in place, the bf16 snapshot of
+//                   the state for the Q S product, the initial and final states
+//   warps 6..9    : output group: causal mask of P = Q K^T into bf16 in place in
+//                   tensor memory (the A operand of P~ W), output rows scaled,
+//                   staged in the chunk's V slot and written by a TMA store
+// Warp w (w >= 2) reads TMEM lanes 32*(w%4) .. +31.
+//
+// Long sequences are cut into segments so that enough CTAs fill the GPU.  A
+// state-only pre-pass (this kernel with SO = true: K and V only) writes each
+// segment's local end state to a float32 workspace; the main pass starts
+// segment s from sum_{t<s} gamma^((s-1-t) Lseg) state_t.  The main pass is
+// launched with programmatic stream serialisation: its CTAs start while the
+// pre-pass runs and only the state group waits (griddepcontrol.wait) before it
+// reads the workspace.
+//
 // Every mbarrier wait gives up after kWaitLimitNs, sets RET_DEV_WAIT_TIMEOUT in
 // the device status word and unwinds: in-flight TMA loads and MMAs are waited
 // for (again with a limit), bulk stores drained and TMEM released.
-//
-// Long sequences are cut into `segments` runs of chunks so that enough CTAs
-// exist to fill the GPU.  A state-only pre-pass (the same kernel without Q, P
-// or outputs) writes each segment's local end state to a float32 workspace;
-// the main pass starts segment s from sum_{t<s} gamma^((s-1-t) Lseg) state_t,
-// the exclusive scan of (gamma^Lseg, state_t) pairs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -48,10 +75,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
-constexpr uint32_t kEpiBarrier = 1;                 // named barrier id of the epilogue warps
+constexpr int kThreads = 320;
+constexpr int kGroup = 128;                         // threads of one epilogue group
+constexpr uint32_t kBarS = 1, kBarO = 2;            // named barrier ids of the two groups
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
+constexpr float kMinChunkDecayLog2 = -14.0f;        // rescaled form: gamma^C >= 2^-14
 
 // Rows of an M=64 accumulator occupy the first 16 lanes of each 32-lane TMEM
 // sub-partition: row 16*q + l lives in lane 32*q + l, l < 16.
@@ -60,53 +88,70 @@ __device__ __forceinline__ int acc_row(int M, int quarter, int lane) {
   return lane < 16 ? 16 * quarter + lane : -1;
 }
 
-template <int C, int DK, int DVT, int NS, bool SO>
+template <int C, int DK, int DVT, bool SO>
 struct Cfg {
   static_assert(C == 64 || C == 128, "chunk");
   static_assert(DK == 128 || DK == 256, "dk");
   static_assert(DVT == 64 || DVT == 128, "value tile");
-  static constexpr int kQ = SO ? 0 : C * DK * 2;
-  static constexpr int kK = C * DK * 2;
-  static constexpr int kV = C * DVT * 2;
-  static constexpr int kStage = kQ + kK + kV;
-  static constexpr int kW = C * DVT * 2;
-  static constexpr int kP = SO ? 0 : C * C * 2;
-  static constexpr int kSb = SO ? 0 : DK * DVT * 2;
-  static constexpr bool kOsAlias = !SO && DVT <= C;  // output staging reuses the P~ buffer
-  static constexpr int kOs = (SO || kOsAlias) ? 0 : C * DVT * 2;
-  static constexpr int oW = NS * kStage;
-  static constexpr int oP = oW + kW;
-  static constexpr int oSb = oP + kP;
-  static constexpr int oOs = kOsAlias ? oP : oSb + kSb;
-  static constexpr int oPw = oSb + kSb + kOs;
+  static constexpr int H = DK / 128;                  // 128-row halves of the state
+  // shared memory
+  static constexpr int kQ = SO ? 0 : C * 256;         // one 128-column half of Q_i: two 64-column boxes
+  static constexpr int kK = C * 256;                  // the same half of K_i
+  static constexpr int kQK = kQ + kK;
+  static constexpr int kV = C * DVT * 2;              // V_i slab (also W_i, then the output staging)
+  static constexpr int kSb = SO ? 0 : 128 * DVT * 2;  // bf16 snapshot of one state half
   static constexpr int kPw = ((C + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kBarBytes = 64 * 8;
+  static constexpr int bytes(int nqk, int nv) {
+    return nqk * kQK + nv * kV + kSb + kPw + kBarBytes + 16 + 1024;  // + slack to align to 1024
+  }
+  static constexpr int pick_nqk() {
+    int n = 6;
+    while (n > H && bytes(n, n) > kMaxSmemPerBlock) --n;
+    return n;
+  }
+  static constexpr int NQK = pick_nqk();
+  static constexpr int pick_nv() {
+    int v = NQK;
+    while (v < 8 && bytes(NQK, v + 1) <= kMaxSmemPerBlock) ++v;
+    return v;
+  }
+  static constexpr int NV = pick_nv();
+  static_assert(NQK >= H && bytes(NQK, NV) <= kMaxSmemPerBlock, "shared memory");
+  static constexpr int oV = NQK * kQK;
+  static constexpr int oSb = oV + NV * kV;
+  static constexpr int oPw = oSb + kSb;
   static constexpr int oBar = oPw + kPw;
-  // barriers: FULL[NS], EMPTY[NS], P_FULL, P_FREE, SB_READY, PW_READY, O_FULL, O_FREE, S_FULL, FIN
-  static constexpr int kBars = 2 * NS + 8;
-  static constexpr int oSlot = oBar + kBars * 8;
+  static constexpr int oSlot = oBar + kBarBytes;
   static constexpr int oAbort = oSlot + 4;
-  static constexpr int kBytes = oAbort + 4;
-  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
-  static_assert(kAlloc <= kMaxSmemPerBlock, "shared memory");
-  static_assert(kStage % 1024 == 0 && kW % 1024 == 0 && kP % 1024 == 0 && kSb % 1024 == 0, "align");
-  // TMEM columns
-  static constexpr int kSCols = (DK / 128) * DVT;
-  static constexpr int cS = 0, cP = kSCols, cO1 = kSCols + C, cO2 = kSCols + C + DVT;
-  static constexpr int kColsUsed = SO ? kSCols : kSCols + C + 2 * DVT;
+  static constexpr int kAlloc = bytes(NQK, NV);
+  static_assert(kQK % 1024 == 0 && kV % 1024 == 0 && kSb % 1024 == 0, "align");
+  // tensor memory: state halves, P buffers, output buffers
+  static constexpr int kSCols = H * DVT;
+  static constexpr int NP = (!SO && kSCols + 2 * C + DVT <= 512) ? 2 : 1;
+  static constexpr int NO = (!SO && kSCols + NP * C + 2 * DVT <= 512) ? 2 : 1;
+  static constexpr int cS = 0, cP = kSCols, cO = kSCols + NP * C;
+  static constexpr int kColsUsed = SO ? kSCols : cO + NO * DVT;
+  static_assert(kColsUsed <= 512, "tmem");
   static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
                                    : kColsUsed <= 256 ? 256 : 512;
-  static_assert(kColsUsed <= 512, "tmem");
-  // barrier indices
-  static constexpr int bFull = 0, bEmpty = NS, bPFull = 2 * NS, bPFree = 2 * NS + 1,
-                       bSbReady = 2 * NS + 2, bPwReady = 2 * NS + 3, bOFull = 2 * NS + 4,
-                       bOFree = 2 * NS + 5, bSFull = 2 * NS + 6, bFin = 2 * NS + 7;
+  // Q K^T of chunk i+1 is issued before the outputs of chunk i when both
+  // chunks' Q/K halves and P buffers fit at once.
+  static constexpr bool kLookahead = !SO && NQK >= 2 * H && NP >= 2;
+  // barriers
+  static constexpr int bQkFull = 0, bQkEmpty = NQK, bVFull = 2 * NQK, bVEmpty = 2 * NQK + NV,
+                       bWReady = 2 * NQK + 2 * NV, bSRead = 2 * NQK + 3 * NV, bSFull = bSRead + H,
+                       bSbReady = bSFull + H, bSbFree = bSbReady + 1, bPFull = bSbFree + 1,
+                       bPFree = bPFull + NP, bPtReady = bPFree + NP, bOFull = bPtReady + NP,
+                       bOFree = bOFull + NO, bFin = bOFree + NO, kBars = bFin + 1;
+  static_assert(kBars * 8 <= kBarBytes, "barriers");
 };
 
 struct TcParams {
   const float* gamma;
-  float* state_out;  // main pass: final state (may be null); pre-pass: unused
+  float* state_out;  // main pass: final state (may be null)
   float* ws;         // segment states [B*H][segments-1][DK][dv]
-  int H, N, dv, n_dv_tiles, segments, seg_chunks, n_chunks;
+  int H, N, dv, n_dv_tiles, BH, segments, seg_chunks, n_chunks;
   float scale;       // 1/sqrt(dk)
 };
 
@@ -114,6 +159,18 @@ __device__ __forceinline__ float gamma_pow(float g, float lg, float d) {
   if (d == 0.0f) return 1.0f;
   if (g <= 0.0f) return 0.0f;
   return exp2f(d * lg);
+}
+
+// One chunk of the rescaled state's bookkeeping: from c (in [1, 2)) and
+// gamma^L >= 2^-14, n = floor(log2(c / gamma^L)) in [0, 15] and
+// c <- 2^-n c / gamma^L.  Every thread that needs c or n runs the same
+// sequence of these steps, so all of them hold identical values.
+__device__ __forceinline__ void frame_advance(float& c, int& n, float gL) {
+  const float y = __fdiv_rn(c, gL);
+  int e = (int)((__float_as_uint(y) >> 23) & 0xffu) - 127;
+  e = e < 0 ? 0 : (e > 15 ? 15 : e);
+  n = e;
+  c = y * __uint_as_float((uint32_t)(127 - e) << 23);
 }
 
 __device__ __forceinline__ void flag_timeout(volatile int* abort_flag) {
@@ -146,11 +203,12 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Epilogue-wide wait: every epilogue thread waits, then all agree (one
-// barrier with an OR) on whether to go on, so the warps never diverge.
-__device__ __forceinline__ bool epi_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// Group-wide wait: every thread of an epilogue group waits, then all agree
+// (one barrier with an OR) on whether to go on, so the warps never diverge.
+__device__ __forceinline__ bool group_wait(uint32_t id, uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag) {
   const bool ok = wait_bar(bar, parity, abort_flag);
-  return !named_bar_or(kEpiBarrier, kEpiThreads, !ok || *abort_flag);
+  return !named_bar_or(id, kGroup, !ok || *abort_flag);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -158,70 +216,102 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Store 32 fp32 values (columns col0..col0+31, col0 % 32 == 0) of row `row` as
-// bf16 into a 128-byte-swizzled tile made of 64-column blocks of `rows_per_block` rows.
-__device__ __forceinline__ void store_row32_swz(uint8_t* tile, int rows_per_block, int row, int col0,
-                                                const float (&x)[32]) {
+// Columns col0..col0+31 (col0 % 32 == 0) of row `row`, as 16 packed bf16
+// pairs, into a 128-byte-swizzled tile made of 64-column blocks of
+// `rows_per_block` rows (the layout of a TMA SWIZZLE_128B box).
+__device__ __forceinline__ void store_row32_packed(uint8_t* tile, int rows_per_block, int row,
+                                                   int col0, const uint32_t* pk) {
   uint8_t* blk = tile + (col0 / 64) * rows_per_block * 128;
   const int c16 = (col0 % 64) / 8;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 v;
-    v.x = pack_bf16(x[8 * j + 0], x[8 * j + 1]);
-    v.y = pack_bf16(x[8 * j + 2], x[8 * j + 3]);
-    v.z = pack_bf16(x[8 * j + 4], x[8 * j + 5]);
-    v.w = pack_bf16(x[8 * j + 6], x[8 * j + 7]);
-    *reinterpret_cast<uint4*>(blk + swz128(row, c16 + j)) = v;
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(blk + swz128(row, c16 + j)) =
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
+// Multiply, in place, every bf16 element of row r of a tile of 128-byte rows
+// (`rows` rows per 64-column box, `nbytes` in total) by f(r).
+template <class F>
+__device__ __forceinline__ void scale_rows_bf16(uint8_t* base, int nbytes, int rows, int tid, F f) {
+#pragma unroll 4
+  for (int off = tid * 16; off < nbytes; off += kGroup * 16) {
+    const int row = (off % (rows * 128)) / 128;
+    const float s = f(row);
+    uint4 v = *reinterpret_cast<const uint4*>(base + off);
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 t = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
+      w[j] = pack_bf16(t.x * s, t.y * s);
+    }
+    *reinterpret_cast<uint4*>(base + off) = v;
   }
 }
 
-template <int C, int DK, int DVT, int NS, bool SO>
+template <int C, int DK, int DVT, bool SO>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                 const TcParams p) {
-  using L = Cfg<C, DK, DVT, NS, SO>;
+  using L = Cfg<C, DK, DVT, SO>;
+  constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
-  float* pw = reinterpret_cast<float*>(sm + L::oPw);
+  float* pw = reinterpret_cast<float*>(sm + L::oPw);  // pw[d] = gamma^d, d = 0..C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oSlot);
   auto bar = [&](int i) { return sbase + L::oBar + 8 * i; };
-  auto stage_q = [&](int s) { return sbase + s * L::kStage; };
-  auto stage_k = [&](int s) { return sbase + s * L::kStage + L::kQ; };
-  auto stage_v = [&](int s) { return sbase + s * L::kStage + L::kQ + L::kK; };
+  auto qk_q = [&](int s) { return sbase + s * L::kQK; };
+  auto qk_k = [&](int s) { return sbase + s * L::kQK + L::kQ; };
+  auto v_slot = [&](int s) { return sbase + L::oV + s * L::kV; };
+  const uint32_t sSb = sbase + L::oSb;
 
-  // ---- work item ----
-  const int segs_in_grid = SO ? p.segments - 1 : p.segments;
+  // ---- work item: (dv tile fastest, then head, then segment) ----
   int idx = blockIdx.x;
   const int dvt = idx % p.n_dv_tiles;
   idx /= p.n_dv_tiles;
-  const int seg = idx % segs_in_grid;
-  const int bh = idx / segs_in_grid;
-  const int h = bh % p.H;
+  const int bh = idx % p.BH;
+  const int seg = idx / p.BH;
+  const int head = bh % p.H;
   const int c_begin = seg * p.seg_chunks;
-  const int c_end = min(c_begin + p.seg_chunks, p.n_chunks);
-  const int nck = c_end - c_begin;
+  const int nck = min(c_begin + p.seg_chunks, p.n_chunks) - c_begin;
   const int dv0 = dvt * DVT;
-  const float g = p.gamma[h];
+  const float g = p.gamma[head];
   const float lg = g > 0.f ? log2f(g) : 0.f;
+  const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
+  const bool zero_init = SO || seg == 0;
+  const bool look = L::kLookahead && fast;
+  auto chunk_len = [&](int i) { return min(C, p.N - (c_begin + i) * C); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- set-up ----
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(L::bFull + i), 1);
-      mbar_init(bar(L::bEmpty + i), 1);
+    for (int i = 0; i < NQK; ++i) {
+      mbar_init(bar(L::bQkFull + i), 1);
+      mbar_init(bar(L::bQkEmpty + i), 1);
     }
-    mbar_init(bar(L::bPFull), 1);
-    mbar_init(bar(L::bPFree), kEpiThreads);
-    mbar_init(bar(L::bSbReady), kEpiThreads);
-    mbar_init(bar(L::bPwReady), kEpiThreads);
-    mbar_init(bar(L::bOFull), 1);
-    mbar_init(bar(L::bOFree), kEpiThreads);
-    mbar_init(bar(L::bSFull), 1);
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(bar(L::bVFull + i), 1);
+      mbar_init(bar(L::bVEmpty + i), 1);
+      mbar_init(bar(L::bWReady + i), kGroup);
+    }
+    for (int i = 0; i < H; ++i) {
+      mbar_init(bar(L::bSRead + i), kGroup);
+      mbar_init(bar(L::bSFull + i), 1);
+    }
+    mbar_init(bar(L::bSbReady), kGroup);
+    mbar_init(bar(L::bSbFree), 1);
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(bar(L::bPFull + i), 1);
+      mbar_init(bar(L::bPFree + i), 1);
+      mbar_init(bar(L::bPtReady + i), kGroup);
+    }
+    for (int i = 0; i < NO; ++i) {
+      mbar_init(bar(L::bOFull + i), 1);
+      mbar_init(bar(L::bOFree + i), kGroup);
+    }
     mbar_init(bar(L::bFin), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -239,32 +329,53 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The main pass may start its CTAs now.  This comes after the TMEM
+  // allocation, so a main-pass CTA that lands on this SM and waits for this
+  // grid can never hold the columns this CTA still needs.
+  if (SO) griddep_launch_dependents();
 
   if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
-      int issued = 0;
-      for (int li = 0; li < nck; ++li) {
-        const int s = li % NS, n = li / NS;
-        if (li >= NS && !wait_bar(bar(L::bEmpty + s), (n - 1) & 1, abort_flag)) break;
-        const int row = (c_begin + li) * C;
-        mbar_arrive_expect_tx(bar(L::bFull + s), L::kStage);
-        if (!SO) {
+      int v_issued = 0, qk_issued = 0;
+      bool ok = true;
+      for (int i = 0; i < nck && ok; ++i) {
+        const int row = (c_begin + i) * C;
+        {
+          const int s = i % NV, k = i / NV;
+          if (k > 0 && !wait_bar(bar(L::bVEmpty + s), (k - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::bVFull + s), L::kV);
 #pragma unroll
-          for (int b = 0; b < DK / 64; ++b)
-            tma_load_3d(stage_q(s) + b * C * 128, &tmq, b * 64, row, bh, bar(L::bFull + s));
+          for (int b = 0; b < DVT / 64; ++b)
+            tma_load_3d(v_slot(s) + b * C * 128, &tmv, dv0 + b * 64, row, bh, bar(L::bVFull + s));
+          v_issued = i + 1;
         }
+        for (int hh = 0; hh < H; ++hh) {
+          const int u = i * H + hh, s = u % NQK, k = u / NQK;
+          if (k > 0 && !wait_bar(bar(L::bQkEmpty + s), (k - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(L::bQkFull + s), L::kQK);
+          if (!SO) {
 #pragma unroll
-        for (int b = 0; b < DK / 64; ++b)
-          tma_load_3d(stage_k(s) + b * C * 128, &tmk, b * 64, row, bh, bar(L::bFull + s));
+            for (int b = 0; b < 2; ++b)
+              tma_load_3d(qk_q(s) + b * C * 128, &tmq, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
+          }
 #pragma unroll
-        for (int b = 0; b < DVT / 64; ++b)
-          tma_load_3d(stage_v(s) + b * C * 128, &tmv, dv0 + b * 64, row, bh, bar(L::bFull + s));
-        issued = li + 1;
+          for (int b = 0; b < 2; ++b)
+            tma_load_3d(qk_k(s) + b * C * 128, &tmk, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
+          qk_issued = u + 1;
+        }
       }
       // every issued load has landed before the CTA may exit
-      for (int li = issued - 1; li >= 0 && li >= issued - NS; --li)
-        drain_bar(bar(L::bFull + li % NS), (li / NS) & 1, abort_flag);
+      for (int i = v_issued - 1; i >= 0 && i >= v_issued - NV; --i)
+        drain_bar(bar(L::bVFull + i % NV), (i / NV) & 1, abort_flag);
+      for (int u = qk_issued - 1; u >= 0 && u >= qk_issued - NQK; --u)
+        drain_bar(bar(L::bQkFull + u % NQK), (u / NQK) & 1, abort_flag);
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
@@ -272,254 +383,437 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       constexpr uint32_t idP = make_idesc(C, C, false, false);
       constexpr uint32_t idO = make_idesc(C, DVT, false, true);
       constexpr uint32_t idS = make_idesc(128, DVT, true, true);
-      const uint32_t sW = sbase + L::oW, sP = sbase + L::oP, sSb = sbase + L::oSb;
-      for (int li = 0; li < nck; ++li) {
-        const int s = li % NS, n = li / NS;
-        if (!wait_bar(bar(L::bFull + s), n & 1, abort_flag)) break;
+      int qk_waited = 0;
+      auto wait_qk = [&](int u) -> bool {
+        while (qk_waited <= u) {
+          if (!wait_bar(bar(L::bQkFull + qk_waited % NQK), (qk_waited / NQK) & 1, abort_flag)) return false;
+          ++qk_waited;
+        }
         tc_fence_after();
-        const uint32_t sQ = stage_q(s), sK = stage_k(s), sV = stage_v(s);
-        if (!SO) {
-          if (li > 0 && !wait_bar(bar(L::bPFree), (li - 1) & 1, abort_flag)) break;
-          tc_fence_after();
+        return true;
+      };
+      // P[j % NP] = Q_j K_j^T
+      auto issue_p = [&](int j) -> bool {
+        const int pb = j % NP, kp = j / NP;
+        if (kp > 0 && !wait_bar(bar(L::bPFree + pb), (kp - 1) & 1, abort_flag)) return false;
+        for (int hh = 0; hh < H; ++hh) {
+          const int u = j * H + hh;
+          if (!wait_qk(u)) return false;
+          const int s = u % NQK;
 #pragma unroll
-          for (int kk = 0; kk < DK / 16; ++kk) {
+          for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk / 4) * C * 128 + (kk % 4) * 32;
-            mma_bf16(tmem + L::cP, make_sdesc(sQ + off, 16, 1024), make_sdesc(sK + off, 16, 1024), idP,
-                     kk > 0);
-          }
-          mma_commit(bar(L::bPFull));
-          if (!wait_bar(bar(L::bSbReady), li & 1, abort_flag)) break;
-          if (li > 0 && !wait_bar(bar(L::bOFree), (li - 1) & 1, abort_flag)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < DK / 16; ++kk) {
-            const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
-            mma_bf16(tmem + L::cO1, make_sdesc(sQ + aoff, 16, 1024),
-                     make_sdesc(sSb + kk * 2048, DK * 128, 1024), idO, kk > 0);
-          }
-          if (!wait_bar(bar(L::bPwReady), li & 1, abort_flag)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk) {
-            const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
-            mma_bf16(tmem + L::cO2, make_sdesc(sP + aoff, 16, 1024),
-                     make_sdesc(sV + kk * 2048, C * 128, 1024), idO, kk > 0);
-          }
-          mma_commit(bar(L::bOFull));
-        } else {
-          if (!wait_bar(bar(L::bSbReady), li & 1, abort_flag)) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int half = 0; half < DK / 128; ++half) {
-#pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk) {
-            mma_bf16(tmem + L::cS + half * DVT,
-                     make_sdesc(sK + half * 2 * C * 128 + kk * 2048, C * 128, 1024),
-                     make_sdesc(sW + kk * 2048, C * 128, 1024), idS, 1u);
+            mma_bf16(tmem + L::cP + pb * C, make_sdesc(qk_q(s) + off, 16, 1024),
+                     make_sdesc(qk_k(s) + off, 16, 1024), idP, (hh > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        mma_commit(bar(L::bSFull));
-        mma_commit(bar(L::bEmpty + s));
+        mma_commit(bar(L::bPFull + pb));
+        return true;
+      };
+      // S_h = 2^-n S_h + K_h^T W  (or S_h = K_h^T W when the state is zero)
+      auto issue_s = [&](int i, int n, bool has_state, bool wait_read, bool commit_full) -> bool {
+        const int vs = i % NV;
+        for (int hh = 0; hh < H; ++hh) {
+          const int u = i * H + hh;
+          if (!wait_qk(u)) return false;
+          if (wait_read && !wait_bar(bar(L::bSRead + hh), i & 1, abort_flag)) return false;
+          tc_fence_after();
+          const int s = u % NQK;
+          const uint32_t d = tmem + L::cS + hh * DVT;
+#pragma unroll
+          for (int kk = 0; kk < C / 16; ++kk) {
+            const uint64_t a = make_sdesc(qk_k(s) + kk * 2048, C * 128, 1024);
+            const uint64_t b = make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024);
+            if (kk > 0) mma_bf16(d, a, b, idS, 1u);
+            else if (has_state) mma_bf16_scaled(d, a, b, idS, n);
+            else mma_bf16(d, a, b, idS, 0u);
+          }
+          if (commit_full) mma_commit(bar(L::bSFull + hh));
+        }
+        return true;
+      };
+      // O[i % NO] = sum_h Q_h Sb_h + P~ W
+      auto issue_o = [&](int i, bool has_state) -> bool {
+        const int ob = i % NO, ko = i / NO;
+        if (ko > 0 && !wait_bar(bar(L::bOFree + ob), (ko - 1) & 1, abort_flag)) return false;
+        const uint32_t d = tmem + L::cO + ob * DVT;
+        for (int hh = 0; hh < H; ++hh) {
+          const int u = i * H + hh;
+          if (!wait_bar(bar(L::bSbReady), u & 1, abort_flag)) return false;
+          tc_fence_after();
+          const int s = u % NQK;
+          if (has_state) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
+              mma_bf16(d, make_sdesc(qk_q(s) + aoff, 16, 1024), make_sdesc(sSb + kk * 2048, 128 * 128, 1024),
+                       idO, (hh > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(bar(L::bSbFree));
+          mma_commit(bar(L::bQkEmpty + s));
+        }
+        const int pb = i % NP, vs = i % NV;
+        if (!wait_bar(bar(L::bPtReady + pb), (i / NP) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16_ta(d, tmem + L::cP + pb * C + kk * 8, make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024), idO,
+                      (has_state || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::bOFull + ob));
+        mma_commit(bar(L::bPFree + pb));
+        return true;
+      };
+
+      float c = 1.f;
+      int n = 0;
+      bool ok = true;
+      if (SO) {
+        for (int i = 0; i < nck && ok; ++i) {
+          const int vs = i % NV;
+          if (fast) {
+            frame_advance(c, n, pw[chunk_len(i)]);
+            if (!wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
+            if (!issue_s(i, n, i > 0, false, i == nck - 1)) { ok = false; break; }
+          } else {
+            if (!wait_bar(bar(L::bVFull + vs), (i / NV) & 1, abort_flag) ||
+                !wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
+            if (!issue_s(i, 0, i > 0, true, true)) { ok = false; break; }
+          }
+          for (int hh = 0; hh < H; ++hh) mma_commit(bar(L::bQkEmpty + (i * H + hh) % NQK));
+          mma_commit(bar(L::bVEmpty + vs));
+        }
+      } else {
+        if (look && nck > 0 && !issue_p(0)) ok = false;
+        for (int i = 0; i < nck && ok; ++i) {
+          const bool has_state = i > 0 || !zero_init;
+          const int vs = i % NV;
+          if (fast) {
+            frame_advance(c, n, pw[chunk_len(i)]);
+            if (!wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
+            if (!issue_s(i, n, has_state, true, true)) { ok = false; break; }
+            if (look) {
+              if (i + 1 < nck && !issue_p(i + 1)) { ok = false; break; }
+            } else if (!issue_p(i)) { ok = false; break; }
+          } else {
+            if (!issue_p(i)) { ok = false; break; }
+            if (!wait_bar(bar(L::bVFull + vs), (i / NV) & 1, abort_flag) ||
+                !wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
+            if (!issue_s(i, 0, has_state, true, true)) { ok = false; break; }
+          }
+          if (!issue_o(i, has_state)) { ok = false; break; }
+        }
       }
       // every issued MMA has completed before TMEM is released
       mma_commit(bar(L::bFin));
       drain_bar(bar(L::bFin), 0, abort_flag);
     }
-  } else {
-    // ================= epilogue (warps 2..5) =================
+  } else if (warp < 6) {
+    // ================= state group (warps 2..5) =================
     const int et = threadIdx.x - 64;
     const int quarter = warp & 3;
     const uint32_t lane_addr = (uint32_t)(32 * quarter) << 16;
-    const int srow = 32 * quarter + lane;  // state row (and row of M=128 accumulators)
-    const int arow = acc_row(C, quarter, lane);  // row of the C-row accumulators (P, O1, O2)
-    const uint32_t tS = tmem + lane_addr + L::cS;
-    uint8_t* sW = sm + L::oW;
+    const int srow = 32 * quarter + lane;  // state row inside a 128-row half
+    auto gw = [&](int b, uint32_t par) { return group_wait(kBarS, bar(b), par, abort_flag); };
 
-    // initial state: zero, or (main pass, segment > 0) the decayed sum of the
-    // preceding segments' local states
-    {
+    // initial state of a later segment: the decayed sum of the preceding
+    // segments' local end states (written by the pre-pass)
+    if (!zero_init) {
+      griddep_wait();
       const float* ws_head = p.ws + (size_t)bh * (p.segments - 1) * DK * p.dv;
       const float seg_len = (float)p.seg_chunks * (float)C;
 #pragma unroll 1
-      for (int half = 0; half < DK / 128; ++half) {
-        const int row = half * 128 + srow;
+      for (int hh = 0; hh < H; ++hh) {
+        const int row = hh * 128 + srow;
 #pragma unroll 1
         for (int cb = 0; cb < DVT / 32; ++cb) {
           float acc[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-          if (!SO) {
-            for (int t = 0; t < seg; ++t) {
-              const float f = gamma_pow(g, lg, (float)(seg - 1 - t) * seg_len);
-              const float4* src = reinterpret_cast<const float4*>(
-                  ws_head + ((size_t)t * DK + row) * p.dv + dv0 + cb * 32);
+          for (int t = 0; t < seg; ++t) {
+            const float f = gamma_pow(g, lg, (float)(seg - 1 - t) * seg_len);
+            const float4* src =
+                reinterpret_cast<const float4*>(ws_head + ((size_t)t * DK + row) * p.dv + dv0 + cb * 32);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 x = src[j];
-                acc[4 * j + 0] = fmaf(f, x.x, acc[4 * j + 0]);
-                acc[4 * j + 1] = fmaf(f, x.y, acc[4 * j + 1]);
-                acc[4 * j + 2] = fmaf(f, x.z, acc[4 * j + 2]);
-                acc[4 * j + 3] = fmaf(f, x.w, acc[4 * j + 3]);
-              }
+            for (int j = 0; j < 8; ++j) {
+              const float4 x = src[j];
+              acc[4 * j + 0] = fmaf(f, x.x, acc[4 * j + 0]);
+              acc[4 * j + 1] = fmaf(f, x.y, acc[4 * j + 1]);
+              acc[4 * j + 2] = fmaf(f, x.z, acc[4 * j + 2]);
+              acc[4 * j + 3] = fmaf(f, x.w, acc[4 * j + 3]);
             }
           }
           uint32_t r[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
-          tmem_st32(tS + half * DVT + cb * 32, r);
+          tmem_st32(tmem + lane_addr + L::cS + hh * DVT + cb * 32, r);
         }
       }
       tmem_wait_st();
     }
 
-    bool alive = true;
-    for (int li = 0; li < nck && alive; ++li) {
-      const int s = li % NS, n = li / NS;
-      const int row0 = (c_begin + li) * C;
-      const int len = min(C, p.N - row0);
-      const float gL = pw[len];
-
-      // ---- S round trip: bf16 copy of S_{i-1} for Q S, then S <- gamma^L S ----
-      if (li > 0) {
-        if (!epi_wait(bar(L::bSFull), (li - 1) & 1, abort_flag)) { alive = false; break; }
-        tc_fence_after();
+    // W = diag(c gamma^(L-1-m)) V, in place in the chunk's V slot
+    auto w_pass = [&](int i, float ci) -> bool {
+      const int vs = i % NV;
+      if (!gw(L::bVFull + vs, (i / NV) & 1)) return false;
+      const int len = chunk_len(i);
+      scale_rows_bf16(sm + L::oV + vs * L::kV, L::kV, C, et,
+                      [&](int r) { return r < len ? ci * pw[len - 1 - r] : 0.f; });
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::bWReady + vs));
+      return true;
+    };
+    // direct form: K <- diag(gamma^(L-1-m)) K and Q <- diag(scale gamma^(t+1)) Q in place
+    auto kq_pass = [&](int i) -> bool {
+      const int len = chunk_len(i);
+      if (SO) {
+        for (int hh = 0; hh < H; ++hh) {
+          const int u = i * H + hh;
+          if (!gw(L::bQkFull + u % NQK, (u / NQK) & 1)) return false;
+        }
+      } else if (!gw(L::bPFull + i % NP, (i / NP) & 1)) {
+        return false;
       }
+      for (int hh = 0; hh < H; ++hh) {
+        const int s = (i * H + hh) % NQK;
+        scale_rows_bf16(sm + s * L::kQK + L::kQ, L::kK, C, et,
+                        [&](int r) { return r < len ? pw[len - 1 - r] : 0.f; });
+        if (!SO)
+          scale_rows_bf16(sm + s * L::kQK, L::kQ, C, et,
+                          [&](int r) { return r < len ? p.scale * pw[r + 1] : 0.f; });
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::bWReady + i % NV));
+      return true;
+    };
+    // bf16 copy of the state for the Q S product of chunk i (times 2^-n in the
+    // rescaled form; the direct form also decays the state by gamma^L here)
+    auto snapshot = [&](int i, int n, float gL) -> bool {
+      const bool has_state = i > 0 || !zero_init;
+      const float f = __uint_as_float((uint32_t)(127 - n) << 23);  // 2^-n
 #pragma unroll 1
-      for (int half = 0; half < DK / 128; ++half) {
+      for (int hh = 0; hh < H; ++hh) {
+        uint32_t pk[DVT / 2];
+        const uint32_t tS = tmem + lane_addr + L::cS + hh * DVT;
+        if (has_state) {
+          if (i > 0 && !gw(L::bSFull + hh, (i - 1) & 1)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int cb = 0; cb < DVT / 32; ++cb) {
+            uint32_t r[32];
+            tmem_ld32(tS + cb * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[cb * 16 + j] = pack_bf16(f * __uint_as_float(r[2 * j]), f * __uint_as_float(r[2 * j + 1]));
+            if (!fast) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gL);
+              tmem_st32(tS + cb * 32, r);
+            }
+          }
+          if (!fast) tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::bSRead + hh));
+        const int u = i * H + hh;
+        if (u > 0 && !gw(L::bSbFree, (u - 1) & 1)) return false;
+        if (has_state) {
+#pragma unroll
+          for (int cb = 0; cb < DVT / 32; ++cb) store_row32_packed(sm + L::oSb, 128, srow, cb * 32, &pk[cb * 16]);
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(bar(L::bSbReady));
+      }
+      return true;
+    };
+    // final state of this CTA's run of chunks: S^ / c
+    auto final_state = [&](float inv_c, uint32_t parity) {
+      float* dst = nullptr;
+      if (SO) dst = p.ws + ((size_t)bh * (p.segments - 1) + seg) * DK * p.dv;
+      else if (seg == p.segments - 1 && p.state_out) dst = p.state_out + (size_t)bh * DK * p.dv;
+      if (!dst) return;
+#pragma unroll 1
+      for (int hh = 0; hh < H; ++hh) {
+        if (!gw(L::bSFull + hh, parity)) return;
+        tc_fence_after();
 #pragma unroll 1
         for (int cb = 0; cb < DVT / 32; ++cb) {
           uint32_t r[32];
-          tmem_ld32(tS + half * DVT + cb * 32, r);
+          tmem_ld32(tmem + lane_addr + L::cS + hh * DVT + cb * 32, r);
           tmem_wait_ld();
-          float x[32];
+          float4* o = reinterpret_cast<float4*>(dst + (size_t)(hh * 128 + srow) * p.dv + dv0 + cb * 32);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-          if (!SO) store_row32_swz(sm + L::oSb, DK, half * 128 + srow, cb * 32, x);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * gL);
-          tmem_st32(tS + half * DVT + cb * 32, r);
+          for (int j = 0; j < 8; ++j)
+            o[j] = make_float4(__uint_as_float(r[4 * j]) * inv_c, __uint_as_float(r[4 * j + 1]) * inv_c,
+                               __uint_as_float(r[4 * j + 2]) * inv_c, __uint_as_float(r[4 * j + 3]) * inv_c);
         }
       }
-      tmem_wait_st();
-      if (!SO) {
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(L::bSbReady));
-      }
+    };
 
-      // ---- W = diag(gamma^(L-1-j)) V ----
-      if (!epi_wait(bar(L::bFull + s), n & 1, abort_flag)) { alive = false; break; }
-      {
-        const uint8_t* sV = sm + (stage_v(s) - sbase);
-#pragma unroll 2
-        for (int q16 = et; q16 < L::kV / 16; q16 += kEpiThreads) {
-          const int off = q16 * 16;
-          const int row = (off % (C * 128)) / 128;
-          const float f = row < len ? pw[len - 1 - row] : 0.f;
-          uint4 v = *reinterpret_cast<const uint4*>(sV + off);
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+    float c = 1.f;
+    int n = 0;
+    bool alive = true;
+    if (SO) {
+      if (fast) {
+        for (int i = 0; i < nck && alive; ++i) {
+          frame_advance(c, n, pw[chunk_len(i)]);
+          alive = w_pass(i, c);
+        }
+        if (alive && nck > 0) final_state(1.f / c, 0);
+      } else {
+        for (int i = 0; i < nck && alive; ++i) {
+          if (!kq_pass(i)) { alive = false; break; }
+          // decay the carried state by gamma^L (zero before the first chunk)
+          if (i > 0) {
+            const float gL = pw[chunk_len(i)];
+#pragma unroll 1
+            for (int hh = 0; hh < H && alive; ++hh) {
+              if (!gw(L::bSFull + hh, (i - 1) & 1)) { alive = false; break; }
+              tc_fence_after();
+#pragma unroll 1
+              for (int cb = 0; cb < DVT / 32; ++cb) {
+                uint32_t r[32];
+                const uint32_t ta = tmem + lane_addr + L::cS + hh * DVT + cb * 32;
+                tmem_ld32(ta, r);
+                tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float2 t = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
-            w[j] = pack_bf16(t.x * f, t.y * f);
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gL);
+                tmem_st32(ta, r);
+              }
+            }
+            tmem_wait_st();
+            if (!alive) break;
           }
-          *reinterpret_cast<uint4*>(sW + off) = v;
+          tc_fence_before();
+          for (int hh = 0; hh < H; ++hh) mbar_arrive(bar(L::bSRead + hh));
         }
+        if (alive && nck > 0) final_state(1.f, (nck - 1) & 1);
       }
-      fence_proxy_async_smem();
-      if (SO) {
-        tc_fence_before();
-        mbar_arrive(bar(L::bSbReady));
-        continue;
+    } else {
+      if (fast) {
+        float c_next = 1.f;
+        int n_next = 0;
+        if (nck > 0) {
+          frame_advance(c_next, n_next, pw[chunk_len(0)]);
+          alive = w_pass(0, c_next);
+        }
+        for (int i = 0; i < nck && alive; ++i) {
+          c = c_next;
+          n = n_next;
+          if (!snapshot(i, n, 1.f)) { alive = false; break; }
+          if (i + 1 < nck) {
+            frame_advance(c_next, n_next, pw[chunk_len(i + 1)]);
+            if (!w_pass(i + 1, c_next)) { alive = false; break; }
+          }
+        }
+        if (alive && nck > 0) final_state(1.f / c, (nck - 1) & 1);
+      } else {
+        for (int i = 0; i < nck && alive; ++i) {
+          if (!kq_pass(i)) { alive = false; break; }
+          if (!snapshot(i, 0, pw[chunk_len(i)])) { alive = false; break; }
+        }
+        if (alive && nck > 0) final_state(1.f, (nck - 1) & 1);
       }
+    }
+  } else if (!SO) {
+    // ================= output group (warps 6..9) =================
+    const int eo = threadIdx.x - 192;
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = (uint32_t)(32 * quarter) << 16;
+    const int arow = acc_row(C, quarter, lane);  // token row of the C-row accumulators, -1 if none
+    auto go = [&](int b, uint32_t par) { return group_wait(kBarO, bar(b), par, abort_flag); };
 
-      // ---- P~ = (Q K^T (.) D) / sqrt(dk) -> bf16 ----
-      if (L::kOsAlias) {
-        if (et == 0) bulk_wait_group_read0();  // previous output store has read the shared buffer
-        named_bar_sync(kEpiBarrier, kEpiThreads);
-      }
-      if (!epi_wait(bar(L::bPFull), li & 1, abort_flag)) { alive = false; break; }
+    // P~ = causal mask of P (rescaled form) or (P (.) D) scale (direct form),
+    // written as bf16 pairs in place over the first C/2 columns of its buffer
+    auto ptilde = [&](int j) -> bool {
+      const int pb = j % NP;
+      if (!go(L::bPFull + pb, (j / NP) & 1)) return false;
       tc_fence_after();
+      const uint32_t tP = tmem + lane_addr + L::cP + pb * C;
 #pragma unroll 1
       for (int cb = 0; cb < C / 32; ++cb) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + L::cP + cb * 32, r);
+        tmem_ld32(tP + cb * 32, r);
         tmem_wait_ld();
-        if (arow >= 0) {
-          float x[32];
+        uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = cb * 32 + j;
-            x[j] = (c <= arow) ? pw[arow - c] * p.scale * __uint_as_float(r[j]) : 0.f;
+        for (int jj = 0; jj < 16; ++jj) {
+          const int c0 = cb * 32 + 2 * jj;
+          float a = __uint_as_float(r[2 * jj]), b = __uint_as_float(r[2 * jj + 1]);
+          if (fast) {
+            a = c0 <= arow ? a : 0.f;
+            b = c0 + 1 <= arow ? b : 0.f;
+          } else {
+            a = c0 <= arow ? pw[arow - c0] * p.scale * a : 0.f;
+            b = c0 + 1 <= arow ? pw[arow - c0 - 1] * p.scale * b : 0.f;
           }
-          store_row32_swz(sm + L::oP, C, arow, cb * 32, x);
+          pk[jj] = pack_bf16(a, b);
         }
+        tmem_st16(tP + cb * 16, pk);
       }
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::bPFree));
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::bPwReady));
-
-      // ---- out = O2 + diag(gamma^(j+1)) O1 / sqrt(dk) ----
-      if (!epi_wait(bar(L::bOFull), li & 1, abort_flag)) { alive = false; break; }
+      mbar_arrive(bar(L::bPtReady + pb));
+      return true;
+    };
+    // out rows = O rows scaled, bf16, staged in the chunk's V slot, TMA-stored
+    auto out_chunk = [&](int i, float ci) -> bool {
+      const int ob = i % NO;
+      if (!go(L::bOFull + ob, (i / NO) & 1)) return false;
       tc_fence_after();
-      if (!L::kOsAlias) {
-        if (et == 0) bulk_wait_group_read0();
-        named_bar_sync(kEpiBarrier, kEpiThreads);
-      }
-      const float zs = arow >= 0 ? pw[arow + 1] * p.scale : 0.f;
+      const int len = chunk_len(i);
+      float rt = 0.f;
+      if (arow >= 0 && arow < len) rt = fast ? p.scale / (ci * pw[len - 1 - arow]) : 1.f;
+      const int vs = i % NV;
+      uint8_t* stg = sm + L::oV + vs * L::kV;
+      const uint32_t tO = tmem + lane_addr + L::cO + ob * DVT;
 #pragma unroll 1
       for (int cb = 0; cb < DVT / 32; ++cb) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_addr + L::cO1 + cb * 32, a);
-        tmem_ld32(tmem + lane_addr + L::cO2 + cb * 32, b);
+        uint32_t r[32];
+        tmem_ld32(tO + cb * 32, r);
         tmem_wait_ld();
         if (arow >= 0) {
-          float x[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = fmaf(zs, __uint_as_float(a[j]), __uint_as_float(b[j]));
-          store_row32_swz(sm + L::oOs, C, arow, cb * 32, x);
+          for (int jj = 0; jj < 16; ++jj)
+            pk[jj] = pack_bf16(rt * __uint_as_float(r[2 * jj]), rt * __uint_as_float(r[2 * jj + 1]));
+          store_row32_packed(stg, C, arow, cb * 32, pk);
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(L::bOFree));
+      mbar_arrive(bar(L::bOFree + ob));
       fence_proxy_async_smem();
-      named_bar_sync(kEpiBarrier, kEpiThreads);
-      if (et == 0) {
+      named_bar_sync(kBarO, kGroup);
+      if (eo == 0) {
+        const int row0 = (c_begin + i) * C;
 #pragma unroll
-        for (int b = 0; b < DVT / 64; ++b)
-          tma_store_3d(&tmo, sbase + L::oOs + b * C * 128, dv0 + b * 64, row0, bh);
+        for (int b = 0; b < DVT / 64; ++b) tma_store_3d(&tmo, v_slot(vs) + b * C * 128, dv0 + b * 64, row0, bh);
         bulk_commit_group();
+        bulk_wait_group_read0();  // the slot may be refilled once the store has read it
+        mbar_arrive(bar(L::bVEmpty + vs));
       }
-    }
+      return true;
+    };
 
-    // ---- final state of this CTA's run of chunks ----
-    if (alive && nck > 0) {
-      if (epi_wait(bar(L::bSFull), (nck - 1) & 1, abort_flag)) {
-        tc_fence_after();
-        float* dst = nullptr;
-        if (SO) dst = p.ws + ((size_t)bh * (p.segments - 1) + seg) * DK * p.dv;
-        else if (seg == p.segments - 1 && p.state_out) dst = p.state_out + (size_t)bh * DK * p.dv;
-#pragma unroll 1
-        for (int half = 0; half < DK / 128; ++half) {
-#pragma unroll 1
-          for (int cb = 0; cb < DVT / 32; ++cb) {
-            uint32_t r[32];
-            tmem_ld32(tS + half * DVT + cb * 32, r);
-            tmem_wait_ld();
-            if (dst) {
-              float4* o = reinterpret_cast<float4*>(dst + (size_t)(half * 128 + srow) * p.dv + dv0 + cb * 32);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            }
-          }
-        }
+    float c = 1.f;
+    int n = 0;
+    bool alive = true;
+    if (look) {
+      if (nck > 0) alive = ptilde(0);
+      for (int i = 0; i < nck && alive; ++i) {
+        if (i + 1 < nck && !ptilde(i + 1)) { alive = false; break; }
+        frame_advance(c, n, pw[chunk_len(i)]);
+        if (!out_chunk(i, c)) { alive = false; break; }
+      }
+    } else {
+      for (int i = 0; i < nck && alive; ++i) {
+        if (!ptilde(i)) { alive = false; break; }
+        if (fast) frame_advance(c, n, pw[chunk_len(i)]);
+        if (!out_chunk(i, c)) { alive = false; break; }
       }
     }
-    if (!SO && et == 0) bulk_wait_group0();
+    if (eo == 0) bulk_wait_group0();
   }
 
   // ---- teardown ----
@@ -567,34 +861,53 @@ bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows) 
   return r == CUDA_SUCCESS;
 }
 
-template <int C, int DK, int DVT, int NS, bool SO>
+template <int C, int DK, int DVT, bool SO>
 cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mo, const TcParams& p, int grid, cudaStream_t s) {
-  using L = Cfg<C, DK, DVT, NS, SO>;
-  auto kern = chunk_tc_kernel<C, DK, DVT, NS, SO>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+                       const CUtensorMap& mo, const TcParams& p, int grid, bool pdl, cudaStream_t s) {
+  using L = Cfg<C, DK, DVT, SO>;
+  auto kern = chunk_tc_kernel<C, DK, DVT, SO>;
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, L::kAlloc, s>>>(mq, mk, mv, mo, p);
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int C, int DK, int DVT, int NS>
+template <int C, int DK, int DVT>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        const CUtensorMap& mo, const TcParams& p, int BH, cudaStream_t s) {
-  if (p.segments > 1) {
-    constexpr int NS_SO = NS + 1;  // the pre-pass holds no Q, P or output buffers
-    cudaError_t e = launch_one<C, DK, DVT, NS_SO, true>(mq, mk, mv, mo, p,
-                                                        BH * (p.segments - 1) * p.n_dv_tiles, s);
+                        const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
+  const bool split = p.segments > 1;
+  if (split) {
+    cudaError_t e = launch_one<C, DK, DVT, true>(mq, mk, mv, mo, p, p.BH * (p.segments - 1) * p.n_dv_tiles,
+                                                 false, s);
     if (e != cudaSuccess) return e;
   }
-  return launch_one<C, DK, DVT, NS, false>(mq, mk, mv, mo, p, BH * p.segments * p.n_dv_tiles, s);
+  return launch_one<C, DK, DVT, false>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
 }
 
-// The (chunk, dk, value-tile, stages) variants compiled into the library.
-int pick_dvt(int chunk, int dk, int dv) {
-  if (dk == 128 && chunk == 64 && dv % 128 == 0) return 128;
-  return 64;
-}
+// The value-tile width used for these sizes.
+int pick_dvt(int dv) { return dv % 128 == 0 ? 128 : 64; }
 
 }  // namespace
 
@@ -603,7 +916,7 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   if (!(dk == 128 || dk == 256)) return false;
   if (dv <= 0 || dv % 64 != 0 || dv > 1024) return false;
   if (N < 0) return false;
-  const int dvt = pick_dvt(chunk, dk, dv);
+  const int dvt = pick_dvt(dv);
   plan->dvt = dvt;
   plan->n_dv_tiles = dv / dvt;
   plan->n_chunks = (N + chunk - 1) / chunk;
@@ -640,15 +953,20 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.N = N;
   p.dv = dv;
   p.n_dv_tiles = plan.n_dv_tiles;
+  p.BH = BH;
   p.segments = plan.segments;
   p.seg_chunks = plan.seg_chunks;
   p.n_chunks = plan.n_chunks;
   p.scale = (float)(1.0 / std::sqrt((double)dk));
-  if (chunk == 64 && dk == 128 && plan.dvt == 128) return launch_pair<64, 128, 128, 2>(mq, mk, mv, mo, p, BH, s);
-  if (chunk == 64 && dk == 128) return launch_pair<64, 128, 64, 2>(mq, mk, mv, mo, p, BH, s);
-  if (chunk == 128 && dk == 128) return launch_pair<128, 128, 64, 2>(mq, mk, mv, mo, p, BH, s);
-  if (chunk == 64 && dk == 256) return launch_pair<64, 256, 64, 2>(mq, mk, mv, mo, p, BH, s);
-  if (chunk == 128 && dk == 256) return launch_pair<128, 256, 64, 1>(mq, mk, mv, mo, p, BH, s);
+  const bool t128 = plan.dvt == 128;
+  if (chunk == 64 && dk == 128) return t128 ? launch_pair<64, 128, 128>(mq, mk, mv, mo, p, s)
+                                            : launch_pair<64, 128, 64>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dk == 128) return t128 ? launch_pair<128, 128, 128>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<128, 128, 64>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dk == 256) return t128 ? launch_pair<64, 256, 128>(mq, mk, mv, mo, p, s)
+                                            : launch_pair<64, 256, 64>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dk == 256) return t128 ? launch_pair<128, 256, 128>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<128, 256, 64>(mq, mk, mv, mo, p, s);
   return cudaErrorNotSupported;
 }
 

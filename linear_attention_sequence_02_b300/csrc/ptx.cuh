@@ -85,6 +85,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- programmatic dependent launch ----------------------------------------------
+// Let the grid launched after this one (with programmatic stream serialisation)
+// start its CTAs once every CTA of this grid has executed this.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid has completed and its memory is visible
+// (returns at once when the launch had no such dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- named barriers -----------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -131,6 +141,50 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.  A is bf16 in tensor memory:
+// row r of an M=128 operand in lane r (an M=64 operand: row 16q+l in lane
+// 32q+l, l < 16), two consecutive K elements per 32-bit column (the lower K
+// index in the low half).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] = A * B^T + 2^-S * D[tmem] (the MMA's scale-input-d operand; S in 0..15).
+template <int S>
+__device__ __forceinline__ void mma_bf16_scale_d(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p, %4;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "n"(S)
+      : "memory");
+}
+// Runtime choice of the immediate scale operand.
+__device__ __forceinline__ void mma_bf16_scaled(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, int s) {
+  switch (s) {
+    case 0: mma_bf16(d_tmem, adesc, bdesc, idesc, 1u); break;
+    case 1: mma_bf16_scale_d<1>(d_tmem, adesc, bdesc, idesc); break;
+    case 2: mma_bf16_scale_d<2>(d_tmem, adesc, bdesc, idesc); break;
+    case 3: mma_bf16_scale_d<3>(d_tmem, adesc, bdesc, idesc); break;
+    case 4: mma_bf16_scale_d<4>(d_tmem, adesc, bdesc, idesc); break;
+    case 5: mma_bf16_scale_d<5>(d_tmem, adesc, bdesc, idesc); break;
+    case 6: mma_bf16_scale_d<6>(d_tmem, adesc, bdesc, idesc); break;
+    case 7: mma_bf16_scale_d<7>(d_tmem, adesc, bdesc, idesc); break;
+    case 8: mma_bf16_scale_d<8>(d_tmem, adesc, bdesc, idesc); break;
+    case 9: mma_bf16_scale_d<9>(d_tmem, adesc, bdesc, idesc); break;
+    case 10: mma_bf16_scale_d<10>(d_tmem, adesc, bdesc, idesc); break;
+    case 11: mma_bf16_scale_d<11>(d_tmem, adesc, bdesc, idesc); break;
+    case 12: mma_bf16_scale_d<12>(d_tmem, adesc, bdesc, idesc); break;
+    case 13: mma_bf16_scale_d<13>(d_tmem, adesc, bdesc, idesc); break;
+    case 14: mma_bf16_scale_d<14>(d_tmem, adesc, bdesc, idesc); break;
+    default: mma_bf16_scale_d<15>(d_tmem, adesc, bdesc, idesc); break;
+  }
+}
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -158,6 +212,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
       "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
       "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -51,6 +51,29 @@ def test_chunkwise_bf16_cases(orc, B, H, N, dk, dv, C):
     assert_close(st, ref_state, TOL_BF16, "chunkwise state")
 
 
+# Decays outside the schedule.  Each head takes the rescaled form when
+# gamma^chunk >= 2^-14 and the direct form otherwise; the values straddle that
+# switch for both chunk sizes (2^(-14/64) = 0.8595, 2^(-14/128) = 0.9270) and
+# include the ends of [0, 1].
+ANY_GAMMAS = [0.0, 0.3, 0.5, 0.85, 0.9, 0.92, 0.93, 0.99, 1.0]
+
+
+@pytest.mark.parametrize("N,dk,dv,C", [
+    (300, 128, 128, 64),
+    (520, 128, 128, 128),
+    (300, 256, 128, 128),
+    (2048, 128, 64, 64),   # split into segments: state-only pre-pass in both forms
+])
+def test_chunkwise_any_decay(orc, N, dk, dv, C):
+    H = len(ANY_GAMMAS)
+    g = torch.tensor(ANY_GAMMAS, dtype=torch.float32)
+    q, k, v = inputs.qkv(1, H, N, dk, dv, 3, torch.bfloat16)
+    ref_out, ref_state = orc.chunkwise(q, k, v, g.double(), C)
+    out, st = run_chunkwise(q, k, v, g, C)
+    assert_close(out, ref_out, TOL_BF16, "chunkwise out, any decay")
+    assert_close(st, ref_state, TOL_BF16, "chunkwise state, any decay")
+
+
 def test_chunkwise_empty_sequence_zero_state():
     B, H, dk, dv = 1, 2, 128, 128
     z = torch.empty(B, H, 0, dk, dtype=torch.bfloat16, device=DEV)
