@@ -102,30 +102,43 @@ struct Cfg {
   static constexpr int kSb = SO ? 0 : 128 * DVT * 2;  // bf16 snapshot of one state half
   static constexpr int kPw = ((C + 1) * 4 + 15) / 16 * 16;
   static constexpr int kBarBytes = 64 * 8;
-  static constexpr int bytes(int nqk, int nv) {
-    return nqk * kQK + nv * kV + kSb + kPw + kBarBytes + 16 + 1024;  // + slack to align to 1024
+  static constexpr int kStg = SO ? 0 : C * DVT * 2;   // output tile staging for the TMA store
+  static constexpr int bytes(int nqk, int nv, int nsb, int nstg) {
+    return nqk * kQK + nv * kV + nsb * kSb + nstg * kStg + kPw + kBarBytes + 16 + 1024;  // + slack to align
   }
+  static constexpr int kMinQK = 3 > 2 * H ? 3 : 2 * H;
+  // Preferred layout: its own output staging buffer and two snapshot buffers,
+  // so that neither V slots nor snapshots wait for output stores; else its own
+  // staging buffer and one snapshot buffer; else (no room) the output tile is
+  // staged in the chunk's V slot.
+  static constexpr bool kSepStage = !SO && bytes(kMinQK, 3, 1, 1) <= kMaxSmemPerBlock;
+  static constexpr int NSB = !SO && kSepStage && bytes(kMinQK, 3, 2, 1) <= kMaxSmemPerBlock ? 2 : 1;
+  static constexpr int NSTG = kSepStage ? 1 : 0;
   static constexpr int pick_nqk() {
     int n = 6;
-    while (n > H && bytes(n, n) > kMaxSmemPerBlock) --n;
+    while (n > H && bytes(n, n, NSB, NSTG) > kMaxSmemPerBlock) --n;
     return n;
   }
   static constexpr int NQK = pick_nqk();
   static constexpr int pick_nv() {
     int v = NQK;
-    while (v < 8 && bytes(NQK, v + 1) <= kMaxSmemPerBlock) ++v;
+    while (v < 8 && bytes(NQK, v + 1, NSB, NSTG) <= kMaxSmemPerBlock) ++v;
     return v;
   }
   static constexpr int NV = pick_nv();
-  static_assert(NQK >= H && bytes(NQK, NV) <= kMaxSmemPerBlock, "shared memory");
+  static_assert(NQK >= H && bytes(NQK, NV, NSB, NSTG) <= kMaxSmemPerBlock, "shared memory");
   static constexpr int oV = NQK * kQK;
   static constexpr int oSb = oV + NV * kV;
-  static constexpr int oPw = oSb + kSb;
+  static constexpr int oStg = oSb + NSB * kSb;
+  static constexpr int oPw = oStg + NSTG * kStg;
   static constexpr int oBar = oPw + kPw;
   static constexpr int oSlot = oBar + kBarBytes;
   static constexpr int oAbort = oSlot + 4;
-  static constexpr int kAlloc = bytes(NQK, NV);
+  static constexpr int oCState = oSlot + 8;  // final c of the rescaled state (float)
+  static constexpr int kAlloc = bytes(NQK, NV, NSB, NSTG);
   static_assert(kQK % 1024 == 0 && kV % 1024 == 0 && kSb % 1024 == 0, "align");
+  // state_out is staged through the (then idle) rings: rows of DVT + 4 floats
+  static constexpr int kStageRow = DVT + 4;
   // tensor memory: state halves, P buffers, output buffers
   static constexpr int kSCols = H * DVT;
   static constexpr int NP = (!SO && kSCols + 2 * C + DVT <= 512) ? 2 : 1;
@@ -135,13 +148,15 @@ struct Cfg {
   static_assert(kColsUsed <= 512, "tmem");
   static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
                                    : kColsUsed <= 256 ? 256 : 512;
-  // Q K^T of chunk i+1 is issued before the outputs of chunk i when both
-  // chunks' Q/K halves and P buffers fit at once.
-  static constexpr bool kLookahead = !SO && NQK >= 2 * H && NP >= 2;
+  // The output group handles P of chunk i+1 before the outputs of chunk i when
+  // both chunks' Q/K halves and P buffers fit at once and the V ring (whose
+  // slots also stage the outputs) is deep enough that chunk i+1's loads do not
+  // wait for the store of chunk i-1.
+  static constexpr bool kLookahead = !SO && NQK >= 2 * H && NP >= 2 && NV >= 3;
   // barriers
   static constexpr int bQkFull = 0, bQkEmpty = NQK, bVFull = 2 * NQK, bVEmpty = 2 * NQK + NV,
                        bWReady = 2 * NQK + 2 * NV, bSRead = 2 * NQK + 3 * NV, bSFull = bSRead + H,
-                       bSbReady = bSFull + H, bSbFree = bSbReady + 1, bPFull = bSbFree + 1,
+                       bSbReady = bSFull + H, bSbFree = bSbReady + NSB, bPFull = bSbFree + NSB,
                        bPFree = bPFull + NP, bPtReady = bPFree + NP, bOFull = bPtReady + NP,
                        bOFree = bOFull + NO, bFin = bOFree + NO, kBars = bFin + 1;
   static_assert(kBars * 8 <= kBarBytes, "barriers");
@@ -162,11 +177,12 @@ __device__ __forceinline__ float gamma_pow(float g, float lg, float d) {
 }
 
 // One chunk of the rescaled state's bookkeeping: from c (in [1, 2)) and
-// gamma^L >= 2^-14, n = floor(log2(c / gamma^L)) in [0, 15] and
-// c <- 2^-n c / gamma^L.  Every thread that needs c or n runs the same
-// sequence of these steps, so all of them hold identical values.
-__device__ __forceinline__ void frame_advance(float& c, int& n, float gL) {
-  const float y = __fdiv_rn(c, gL);
+// inv_gL = 1 / gamma^L <= 2^14, n = floor(log2(c inv_gL)) in [0, 15] and
+// c <- 2^-n c inv_gL.  Any consistent value of c is exact for the method (it
+// only rescales the stored state); every thread that needs c or n runs the
+// same sequence of these steps, so all of them hold identical values.
+__device__ __forceinline__ void frame_advance(float& c, int& n, float inv_gL) {
+  const float y = c * inv_gL;
   int e = (int)((__float_as_uint(y) >> 23) & 0xffu) - 127;
   e = e < 0 ? 0 : (e > 15 ? 15 : e);
   n = e;
@@ -230,21 +246,95 @@ __device__ __forceinline__ void store_row32_packed(uint8_t* tile, int rows_per_b
 }
 
 // Multiply, in place, every bf16 element of row r of a tile of 128-byte rows
-// (`rows` rows per 64-column box, `nbytes` in total) by f(r).
-template <class F>
-__device__ __forceinline__ void scale_rows_bf16(uint8_t* base, int nbytes, int rows, int tid, F f) {
-#pragma unroll 4
-  for (int off = tid * 16; off < nbytes; off += kGroup * 16) {
-    const int row = (off % (rows * 128)) / 128;
-    const float s = f(row);
-    uint4 v = *reinterpret_cast<const uint4*>(base + off);
-    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+// (ROWS rows per 64-column box, NBYTES in total) by f(r).  Each of the group's
+// threads loads a batch of up to eight 16-byte units before it scales and
+// stores any, so a batch costs about one shared-memory round trip.
+template <int NBYTES, int ROWS, class F>
+__device__ __forceinline__ void scale_rows_bf16(uint8_t* base, int tid, F f) {
+  static_assert(NBYTES % (16 * kGroup) == 0, "tile size");
+  constexpr int kUnits = NBYTES / (16 * kGroup);
+  constexpr int kBatch = kUnits < 8 ? kUnits : 8;  // at most 32 registers of data in flight
+  static_assert(kUnits % kBatch == 0, "batch");
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 t = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
-      w[j] = pack_bf16(t.x * s, t.y * s);
+  for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) v[k] = *reinterpret_cast<const uint4*>(base + (tid + (k0 + k) * kGroup) * 16);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int row = (((tid + (k0 + k) * kGroup) * 16) % (ROWS * 128)) / 128;
+      const float s = f(row);
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v[k]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 t = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
+        w[j] = pack_bf16(t.x * s, t.y * s);
+      }
     }
-    *reinterpret_cast<uint4*>(base + off) = v;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) *reinterpret_cast<uint4*>(base + (tid + (k0 + k) * kGroup) * 16) = v[k];
+  }
+}
+
+// Final state of a CTA's run of chunks, S^ / c, after every MMA has completed:
+// lane-major into the workspace (pre-pass), or row-major into state_out (last
+// segment of the main pass) through the then idle shared-memory rings, so the
+// global stores are coalesced.  Kept out of line: everything it needs is
+// recomputed from the launch parameters, so no register stays live across the
+// roles for it.
+template <int C, int DK, int DVT, bool SO>
+__device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, uint32_t tmem) {
+  using L = Cfg<C, DK, DVT, SO>;
+  constexpr int H = L::H;
+  int idx = blockIdx.x;
+  const int dvt = idx % p.n_dv_tiles;
+  idx /= p.n_dv_tiles;
+  const int bh = idx % p.BH;
+  const int seg = idx / p.BH;
+  const int nck = min(seg * p.seg_chunks + p.seg_chunks, p.n_chunks) - seg * p.seg_chunks;
+  const bool to_out = !SO && seg == p.segments - 1 && p.state_out != nullptr;
+  if (!(SO || to_out) || nck <= 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dv0 = dvt * DVT;
+  if (warp >= 2 && warp < 6) {
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = (uint32_t)(32 * quarter) << 16;
+    const int srow = 32 * quarter + lane;
+    const float inv_c = 1.f / *reinterpret_cast<const float*>(sm + L::oCState);
+#pragma unroll 1
+    for (int hh = 0; hh < H; ++hh) {
+#pragma unroll 1
+      for (int cb = 0; cb < DVT / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + L::cS + hh * DVT + cb * 32, r);
+        tmem_wait_ld();
+        float4* dst;
+        size_t stride;
+        if (SO) {
+          // float4 number (c4 * 128 + row) of block (bh, segment, dv tile, half)
+          dst = reinterpret_cast<float4*>(p.ws) +
+                ((((size_t)bh * (p.segments - 1) + seg) * p.n_dv_tiles + dvt) * H + hh) * (size_t)(DVT / 4) * 128 +
+                (size_t)(cb * 8) * 128 + srow;
+          stride = 128;
+        } else {
+          dst = reinterpret_cast<float4*>(sm) + ((size_t)(hh * 128 + srow) * L::kStageRow) / 4 + cb * 8;
+          stride = 1;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j * stride] = make_float4(__uint_as_float(r[4 * j]) * inv_c, __uint_as_float(r[4 * j + 1]) * inv_c,
+                                        __uint_as_float(r[4 * j + 2]) * inv_c, __uint_as_float(r[4 * j + 3]) * inv_c);
+      }
+    }
+  }
+  if (to_out) {
+    __syncthreads();
+    const float4* src = reinterpret_cast<const float4*>(sm);
+    float* base = p.state_out + (size_t)bh * DK * p.dv + dv0;
+    for (int q4 = threadIdx.x; q4 < DK * DVT / 4; q4 += kThreads) {
+      const int row = q4 / (DVT / 4), c4 = q4 % (DVT / 4);
+      *reinterpret_cast<float4*>(base + (size_t)row * p.dv + 4 * c4) = src[row * (L::kStageRow / 4) + c4];
+    }
   }
 }
 
@@ -254,9 +344,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                 const TcParams p) {
   using L = Cfg<C, DK, DVT, SO>;
-  constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO;
+  constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Align by pointer arithmetic on the __shared__ array itself (not through an
+  // integer), so the compiler keeps every access below in the shared window.
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(sm);
   float* pw = reinterpret_cast<float*>(sm + L::oPw);  // pw[d] = gamma^d, d = 0..C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oAbort);
@@ -265,7 +357,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   auto qk_q = [&](int s) { return sbase + s * L::kQK; };
   auto qk_k = [&](int s) { return sbase + s * L::kQK + L::kQ; };
   auto v_slot = [&](int s) { return sbase + L::oV + s * L::kV; };
-  const uint32_t sSb = sbase + L::oSb;
+  auto sb_buf = [&](int b) { return sbase + L::oSb + b * L::kSb; };
 
   // ---- work item: (dv tile fastest, then head, then segment) ----
   int idx = blockIdx.x;
@@ -283,8 +375,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   const bool zero_init = SO || seg == 0;
   const bool look = L::kLookahead && fast;
   auto chunk_len = [&](int i) { return min(C, p.N - (c_begin + i) * C); };
+  // Segment states in the workspace are stored lane-major: float4 number
+  // (c4 * 128 + row) of block (bh, segment, dv tile, half) holds columns
+  // 4c4..4c4+3 of state row `row`, so a warp's 32 rows are 512 contiguous bytes.
+  auto ws_block = [&](int s, int hh) {
+    return reinterpret_cast<float4*>(p.ws) +
+           ((((size_t)bh * (p.segments - 1) + s) * p.n_dv_tiles + dvt) * H + hh) * (size_t)(DVT / 4) * 128;
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float inv_gC = 1.f;   // 1 / gamma^C (rescaled form only), set once pw[] is filled
+  auto inv_g = [&](int i) {
+    const int len = chunk_len(i);
+    return len == C ? inv_gC : 1.f / pw[len];
+  };
 
   // ---- set-up ----
   if (threadIdx.x == 0) {
@@ -301,8 +405,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       mbar_init(bar(L::bSRead + i), kGroup);
       mbar_init(bar(L::bSFull + i), 1);
     }
-    mbar_init(bar(L::bSbReady), kGroup);
-    mbar_init(bar(L::bSbFree), 1);
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(bar(L::bSbReady + i), kGroup);
+      mbar_init(bar(L::bSbFree + i), 1);
+    }
     for (int i = 0; i < NP; ++i) {
       mbar_init(bar(L::bPFull + i), 1);
       mbar_init(bar(L::bPFree + i), 1);
@@ -329,6 +435,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (fast) inv_gC = 1.f / pw[C];
   // The main pass may start its CTAs now.  This comes after the TMEM
   // allocation, so a main-pass CTA that lands on this SM and waits for this
   // grid can never hold the columns this CTA still needs.
@@ -383,125 +490,159 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       constexpr uint32_t idP = make_idesc(C, C, false, false);
       constexpr uint32_t idO = make_idesc(C, DVT, false, true);
       constexpr uint32_t idS = make_idesc(128, DVT, true, true);
-      int qk_waited = 0;
-      auto wait_qk = [&](int u) -> bool {
-        while (qk_waited <= u) {
-          if (!wait_bar(bar(L::bQkFull + qk_waited % NQK), (qk_waited / NQK) & 1, abort_flag)) return false;
-          ++qk_waited;
-        }
-        tc_fence_after();
-        return true;
-      };
-      // P[j % NP] = Q_j K_j^T
-      auto issue_p = [&](int j) -> bool {
-        const int pb = j % NP, kp = j / NP;
-        if (kp > 0 && !wait_bar(bar(L::bPFree + pb), (kp - 1) & 1, abort_flag)) return false;
-        for (int hh = 0; hh < H; ++hh) {
-          const int u = j * H + hh;
-          if (!wait_qk(u)) return false;
-          const int s = u % NQK;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk / 4) * C * 128 + (kk % 4) * 32;
-            mma_bf16(tmem + L::cP + pb * C, make_sdesc(qk_q(s) + off, 16, 1024),
-                     make_sdesc(qk_k(s) + off, 16, 1024), idP, (hh > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(bar(L::bPFull + pb));
-        return true;
-      };
+      auto test = [&](int b, int parity) { return mbar_test_wait(bar(b), (uint32_t)(parity & 1)); };
+      auto has_state = [&](int i) { return i > 0 || !zero_init; };
       // S_h = 2^-n S_h + K_h^T W  (or S_h = K_h^T W when the state is zero)
-      auto issue_s = [&](int i, int n, bool has_state, bool wait_read, bool commit_full) -> bool {
-        const int vs = i % NV;
-        for (int hh = 0; hh < H; ++hh) {
-          const int u = i * H + hh;
-          if (!wait_qk(u)) return false;
-          if (wait_read && !wait_bar(bar(L::bSRead + hh), i & 1, abort_flag)) return false;
-          tc_fence_after();
-          const int s = u % NQK;
-          const uint32_t d = tmem + L::cS + hh * DVT;
+      auto mma_s = [&](int i, int hh, int n) {
+        const int s = (i * H + hh) % NQK, vs = i % NV;
+        const uint32_t d = tmem + L::cS + hh * DVT;
 #pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk) {
-            const uint64_t a = make_sdesc(qk_k(s) + kk * 2048, C * 128, 1024);
-            const uint64_t b = make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024);
-            if (kk > 0) mma_bf16(d, a, b, idS, 1u);
-            else if (has_state) mma_bf16_scaled(d, a, b, idS, n);
-            else mma_bf16(d, a, b, idS, 0u);
-          }
-          if (commit_full) mma_commit(bar(L::bSFull + hh));
+        for (int kk = 0; kk < C / 16; ++kk) {
+          const uint64_t a = make_sdesc(qk_k(s) + kk * 2048, C * 128, 1024);
+          const uint64_t b = make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024);
+          if (kk > 0) mma_bf16(d, a, b, idS, 1u);
+          else if (has_state(i)) mma_bf16_scaled(d, a, b, idS, n);
+          else mma_bf16(d, a, b, idS, 0u);
         }
-        return true;
       };
-      // O[i % NO] = sum_h Q_h Sb_h + P~ W
-      auto issue_o = [&](int i, bool has_state) -> bool {
-        const int ob = i % NO, ko = i / NO;
-        if (ko > 0 && !wait_bar(bar(L::bOFree + ob), (ko - 1) & 1, abort_flag)) return false;
-        const uint32_t d = tmem + L::cO + ob * DVT;
-        for (int hh = 0; hh < H; ++hh) {
-          const int u = i * H + hh;
-          if (!wait_bar(bar(L::bSbReady), u & 1, abort_flag)) return false;
-          tc_fence_after();
-          const int s = u % NQK;
-          if (has_state) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
-              mma_bf16(d, make_sdesc(qk_q(s) + aoff, 16, 1024), make_sdesc(sSb + kk * 2048, 128 * 128, 1024),
-                       idO, (hh > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          mma_commit(bar(L::bSbFree));
-          mma_commit(bar(L::bQkEmpty + s));
-        }
-        const int pb = i % NP, vs = i % NV;
-        if (!wait_bar(bar(L::bPtReady + pb), (i / NP) & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16_ta(d, tmem + L::cP + pb * C + kk * 8, make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024), idO,
-                      (has_state || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::bOFull + ob));
-        mma_commit(bar(L::bPFree + pb));
-        return true;
-      };
-
-      float c = 1.f;
-      int n = 0;
       bool ok = true;
       if (SO) {
+        // state only: S in chunk order, each once its W (or K^) and, in the
+        // direct form, the decayed state are ready
+        float c = 1.f;
+        int n = 0, qk_waited = 0;
         for (int i = 0; i < nck && ok; ++i) {
           const int vs = i % NV;
-          if (fast) {
-            frame_advance(c, n, pw[chunk_len(i)]);
-            if (!wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
-            if (!issue_s(i, n, i > 0, false, i == nck - 1)) { ok = false; break; }
-          } else {
-            if (!wait_bar(bar(L::bVFull + vs), (i / NV) & 1, abort_flag) ||
-                !wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
-            if (!issue_s(i, 0, i > 0, true, true)) { ok = false; break; }
+          if (fast) frame_advance(c, n, inv_g(i));
+          if (!wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag) ||
+              (!fast && !wait_bar(bar(L::bVFull + vs), (i / NV) & 1, abort_flag))) {
+            ok = false;
+            break;
           }
-          for (int hh = 0; hh < H; ++hh) mma_commit(bar(L::bQkEmpty + (i * H + hh) % NQK));
-          mma_commit(bar(L::bVEmpty + vs));
+          for (int hh = 0; hh < H && ok; ++hh) {
+            const int u = i * H + hh;
+            while (ok && qk_waited <= u) {
+              ok = wait_bar(bar(L::bQkFull + qk_waited % NQK), (qk_waited / NQK) & 1, abort_flag);
+              ++qk_waited;
+            }
+            if (ok && !fast) ok = wait_bar(bar(L::bSRead + hh), i & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            mma_s(i, hh, n);
+            if (!fast) mma_commit(bar(L::bSFull + hh));
+            mma_commit(bar(L::bQkEmpty + u % NQK));
+          }
+          if (ok) mma_commit(bar(L::bVEmpty + vs));
         }
       } else {
-        if (look && nck > 0 && !issue_p(0)) ok = false;
-        for (int i = 0; i < nck && ok; ++i) {
-          const bool has_state = i > 0 || !zero_init;
-          const int vs = i % NV;
-          if (fast) {
-            frame_advance(c, n, pw[chunk_len(i)]);
-            if (!wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
-            if (!issue_s(i, n, has_state, true, true)) { ok = false; break; }
-            if (look) {
-              if (i + 1 < nck && !issue_p(i + 1)) { ok = false; break; }
-            } else if (!issue_p(i)) { ok = false; break; }
-          } else {
-            if (!issue_p(i)) { ok = false; break; }
-            if (!wait_bar(bar(L::bVFull + vs), (i / NV) & 1, abort_flag) ||
-                !wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag)) { ok = false; break; }
-            if (!issue_s(i, 0, has_state, true, true)) { ok = false; break; }
+        // Four in-order streams, each MMA issued as soon as its operands are
+        // ready, by priority: the state chain, Q S (it frees the snapshot
+        // buffer and the Q/K slot), Q K^T, P~ W.
+        float c = 1.f;
+        int n = 0;
+        int qk_ok = 0;                      // Q/K units known to be loaded
+        int s_i = 0, s_h = 0;               // next state update
+        bool s_w = false;                   // its W (or K^/Q~) is ready
+        int p_j = 0;                        // next Q K^T
+        int oi_i = 0, oi_h = 0;             // next Q S
+        int oa_i = 0;                       // next P~ W
+        auto qk_ready = [&](int u_end) {
+          while (qk_ok < u_end) {
+            if (!test(L::bQkFull + qk_ok % NQK, qk_ok / NQK)) return false;
+            ++qk_ok;
           }
-          if (!issue_o(i, has_state)) { ok = false; break; }
+          return true;
+        };
+        uint64_t t_last = globaltimer_ns();
+        while (oa_i < nck) {
+          bool issued = false;
+          if (s_i < nck) {
+            const int vs = s_i % NV;
+            if (!s_w)
+              s_w = test(L::bWReady + vs, s_i / NV) && (fast || test(L::bVFull + vs, s_i / NV));
+            if (s_w && qk_ready(s_i * H + s_h + 1) && test(L::bSRead + s_h, s_i)) {
+              tc_fence_after();
+              if (s_h == 0 && fast) frame_advance(c, n, inv_g(s_i));
+              mma_s(s_i, s_h, fast ? n : 0);
+              mma_commit(bar(L::bSFull + s_h));
+              if (++s_h == H) {
+                s_h = 0;
+                ++s_i;
+                s_w = false;
+              }
+              issued = true;
+            }
+          }
+          if (!issued && (oi_i < s_i || (oi_i == s_i && oi_h < s_h)) && oi_i < p_j) {
+            // O (+)= Q_h Sb_h once the state update of half h is issued (the
+            // snapshot of the next half may wait for this product to free the
+            // buffer); afterwards the chunk's Q/K half is no longer read
+            const int ob = oi_i % NO, ko = oi_i / NO;
+            const int u = oi_i * H + oi_h, b = u % NSB;
+            if ((oi_h > 0 || ko == 0 || test(L::bOFree + ob, ko - 1)) && test(L::bSbReady + b, u / NSB)) {
+              tc_fence_after();
+              if (has_state(oi_i)) {
+                const int s = u % NQK;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
+                  mma_bf16(tmem + L::cO + ob * DVT, make_sdesc(qk_q(s) + aoff, 16, 1024),
+                           make_sdesc(sb_buf(b) + kk * 2048, 128 * 128, 1024), idO,
+                           (oi_h > 0 || kk > 0) ? 1u : 0u);
+                }
+              }
+              mma_commit(bar(L::bSbFree + b));
+              mma_commit(bar(L::bQkEmpty + u % NQK));
+              if (++oi_h == H) {
+                oi_h = 0;
+                ++oi_i;
+              }
+              issued = true;
+            }
+          }
+          if (!issued && p_j < nck && qk_ready((p_j + 1) * H) &&
+              (p_j < NP || test(L::bPFree + p_j % NP, p_j / NP - 1))) {
+            // P[j % NP] = Q_j K_j^T
+            tc_fence_after();
+            const int pb = p_j % NP;
+            for (int hh = 0; hh < H; ++hh) {
+              const int s = (p_j * H + hh) % NQK;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk / 4) * C * 128 + (kk % 4) * 32;
+                mma_bf16(tmem + L::cP + pb * C, make_sdesc(qk_q(s) + off, 16, 1024),
+                         make_sdesc(qk_k(s) + off, 16, 1024), idP, (hh > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(bar(L::bPFull + pb));
+            ++p_j;
+            issued = true;
+          }
+          if (!issued && oa_i < oi_i && test(L::bPtReady + oa_i % NP, oa_i / NP)) {
+            // O += P~ W, P~ read from tensor memory
+            tc_fence_after();
+            const int ob = oa_i % NO, pb = oa_i % NP, vs = oa_i % NV;
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+              mma_bf16_ta(tmem + L::cO + ob * DVT, tmem + L::cP + pb * C + kk * 8,
+                          make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024), idO,
+                          (has_state(oa_i) || kk > 0) ? 1u : 0u);
+            mma_commit(bar(L::bOFull + ob));
+            mma_commit(bar(L::bPFree + pb));
+            if (L::kSepStage) mma_commit(bar(L::bVEmpty + vs));  // V slot free once the MMAs are done
+            ++oa_i;
+            issued = true;
+          }
+          if (issued) {
+            t_last = globaltimer_ns();
+          } else {
+            nanosleep_ns(32);  // leave the issue slots to the epilogue warps
+            if (*abort_flag) break;
+            if (globaltimer_ns() - t_last > kWaitLimitNs) {
+              flag_timeout(abort_flag);
+              break;
+            }
+          }
         }
       }
       // every issued MMA has completed before TMEM is released
@@ -520,11 +661,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     // segments' local end states (written by the pre-pass)
     if (!zero_init) {
       griddep_wait();
-      const float* ws_head = p.ws + (size_t)bh * (p.segments - 1) * DK * p.dv;
       const float seg_len = (float)p.seg_chunks * (float)C;
 #pragma unroll 1
       for (int hh = 0; hh < H; ++hh) {
-        const int row = hh * 128 + srow;
 #pragma unroll 1
         for (int cb = 0; cb < DVT / 32; ++cb) {
           float acc[32];
@@ -532,11 +671,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           for (int j = 0; j < 32; ++j) acc[j] = 0.f;
           for (int t = 0; t < seg; ++t) {
             const float f = gamma_pow(g, lg, (float)(seg - 1 - t) * seg_len);
-            const float4* src =
-                reinterpret_cast<const float4*>(ws_head + ((size_t)t * DK + row) * p.dv + dv0 + cb * 32);
+            const float4* src = ws_block(t, hh) + (size_t)(cb * 8) * 128 + srow;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float4 x = src[j];
+              const float4 x = src[j * 128];
               acc[4 * j + 0] = fmaf(f, x.x, acc[4 * j + 0]);
               acc[4 * j + 1] = fmaf(f, x.y, acc[4 * j + 1]);
               acc[4 * j + 2] = fmaf(f, x.z, acc[4 * j + 2]);
@@ -557,8 +695,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       const int vs = i % NV;
       if (!gw(L::bVFull + vs, (i / NV) & 1)) return false;
       const int len = chunk_len(i);
-      scale_rows_bf16(sm + L::oV + vs * L::kV, L::kV, C, et,
-                      [&](int r) { return r < len ? ci * pw[len - 1 - r] : 0.f; });
+      scale_rows_bf16<L::kV, C>(sm + L::oV + vs * L::kV, et,
+                                [&](int r) { return r < len ? ci * pw[len - 1 - r] : 0.f; });
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bWReady + vs));
       return true;
@@ -576,11 +714,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       }
       for (int hh = 0; hh < H; ++hh) {
         const int s = (i * H + hh) % NQK;
-        scale_rows_bf16(sm + s * L::kQK + L::kQ, L::kK, C, et,
-                        [&](int r) { return r < len ? pw[len - 1 - r] : 0.f; });
+        scale_rows_bf16<L::kK, C>(sm + s * L::kQK + L::kQ, et,
+                                  [&](int r) { return r < len ? pw[len - 1 - r] : 0.f; });
         if (!SO)
-          scale_rows_bf16(sm + s * L::kQK, L::kQ, C, et,
-                          [&](int r) { return r < len ? p.scale * pw[r + 1] : 0.f; });
+          scale_rows_bf16<(SO ? L::kK : L::kQ), C>(sm + s * L::kQK, et,
+                                                  [&](int r) { return r < len ? p.scale * pw[r + 1] : 0.f; });
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bWReady + i % NV));
@@ -590,65 +728,52 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     // rescaled form; the direct form also decays the state by gamma^L here)
     auto snapshot = [&](int i, int n, float gL) -> bool {
       const bool has_state = i > 0 || !zero_init;
-      const float f = __uint_as_float((uint32_t)(127 - n) << 23);  // 2^-n
 #pragma unroll 1
       for (int hh = 0; hh < H; ++hh) {
-        uint32_t pk[DVT / 2];
         const uint32_t tS = tmem + lane_addr + L::cS + hh * DVT;
+        const int u = i * H + hh, b = u % NSB;
+        uint8_t* sb = sm + L::oSb + b * L::kSb;
+        if (u >= NSB && !gw(L::bSbFree + b, (u / NSB - 1) & 1)) return false;
+        if (has_state && i > 0 && !gw(L::bSFull + hh, (i - 1) & 1)) return false;
         if (has_state) {
-          if (i > 0 && !gw(L::bSFull + hh, (i - 1) & 1)) return false;
           tc_fence_after();
+          const float f = fast ? __uint_as_float((uint32_t)(127 - n) << 23) : 1.f;  // 2^-n
 #pragma unroll
-          for (int cb = 0; cb < DVT / 32; ++cb) {
-            uint32_t r[32];
-            tmem_ld32(tS + cb * 32, r);
+          for (int cb = 0; cb < DVT / 32; cb += 2) {
+            uint32_t r[64];
+            tmem_ld32p(tS + cb * 32, &r[0]);
+            tmem_ld32p(tS + cb * 32 + 32, &r[32]);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[cb * 16 + j] = pack_bf16(f * __uint_as_float(r[2 * j]), f * __uint_as_float(r[2 * j + 1]));
             if (!fast) {
+              // direct form: decay the state by gamma^L in place
+              uint32_t t[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gL);
-              tmem_st32(tS + cb * 32, r);
+              for (int j = 0; j < 32; ++j) t[j] = __float_as_uint(__uint_as_float(r[j]) * gL);
+              tmem_st32(tS + cb * 32, t);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) t[j] = __float_as_uint(__uint_as_float(r[32 + j]) * gL);
+              tmem_st32(tS + cb * 32 + 32, t);
+              if (cb + 2 >= DVT / 32) tmem_wait_st();
             }
-          }
-          if (!fast) tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(L::bSRead + hh));
-        const int u = i * H + hh;
-        if (u > 0 && !gw(L::bSbFree, (u - 1) & 1)) return false;
-        if (has_state) {
+            if (cb + 2 >= DVT / 32) {
+              tc_fence_before();
+              mbar_arrive(bar(L::bSRead + hh));  // the state MMA may overwrite S now
+            }
+            uint32_t pk[32];
 #pragma unroll
-          for (int cb = 0; cb < DVT / 32; ++cb) store_row32_packed(sm + L::oSb, 128, srow, cb * 32, &pk[cb * 16]);
+            for (int j = 0; j < 32; ++j)
+              pk[j] = pack_bf16(f * __uint_as_float(r[2 * j]), f * __uint_as_float(r[2 * j + 1]));
+            store_row32_packed(sb, 128, srow, cb * 32, &pk[0]);
+            store_row32_packed(sb, 128, srow, cb * 32 + 32, &pk[16]);
+          }
           fence_proxy_async_smem();
+        } else {
+          tc_fence_before();
+          mbar_arrive(bar(L::bSRead + hh));
         }
-        mbar_arrive(bar(L::bSbReady));
+        mbar_arrive(bar(L::bSbReady + b));
       }
       return true;
-    };
-    // final state of this CTA's run of chunks: S^ / c
-    auto final_state = [&](float inv_c, uint32_t parity) {
-      float* dst = nullptr;
-      if (SO) dst = p.ws + ((size_t)bh * (p.segments - 1) + seg) * DK * p.dv;
-      else if (seg == p.segments - 1 && p.state_out) dst = p.state_out + (size_t)bh * DK * p.dv;
-      if (!dst) return;
-#pragma unroll 1
-      for (int hh = 0; hh < H; ++hh) {
-        if (!gw(L::bSFull + hh, parity)) return;
-        tc_fence_after();
-#pragma unroll 1
-        for (int cb = 0; cb < DVT / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + L::cS + hh * DVT + cb * 32, r);
-          tmem_wait_ld();
-          float4* o = reinterpret_cast<float4*>(dst + (size_t)(hh * 128 + srow) * p.dv + dv0 + cb * 32);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            o[j] = make_float4(__uint_as_float(r[4 * j]) * inv_c, __uint_as_float(r[4 * j + 1]) * inv_c,
-                               __uint_as_float(r[4 * j + 2]) * inv_c, __uint_as_float(r[4 * j + 3]) * inv_c);
-        }
-      }
     };
 
     float c = 1.f;
@@ -657,10 +782,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     if (SO) {
       if (fast) {
         for (int i = 0; i < nck && alive; ++i) {
-          frame_advance(c, n, pw[chunk_len(i)]);
+          frame_advance(c, n, inv_g(i));
           alive = w_pass(i, c);
         }
-        if (alive && nck > 0) final_state(1.f / c, 0);
       } else {
         for (int i = 0; i < nck && alive; ++i) {
           if (!kq_pass(i)) { alive = false; break; }
@@ -688,14 +812,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           tc_fence_before();
           for (int hh = 0; hh < H; ++hh) mbar_arrive(bar(L::bSRead + hh));
         }
-        if (alive && nck > 0) final_state(1.f, (nck - 1) & 1);
       }
     } else {
       if (fast) {
         float c_next = 1.f;
         int n_next = 0;
         if (nck > 0) {
-          frame_advance(c_next, n_next, pw[chunk_len(0)]);
+          frame_advance(c_next, n_next, inv_g(0));
           alive = w_pass(0, c_next);
         }
         for (int i = 0; i < nck && alive; ++i) {
@@ -703,19 +826,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           n = n_next;
           if (!snapshot(i, n, 1.f)) { alive = false; break; }
           if (i + 1 < nck) {
-            frame_advance(c_next, n_next, pw[chunk_len(i + 1)]);
+            frame_advance(c_next, n_next, inv_g(i + 1));
             if (!w_pass(i + 1, c_next)) { alive = false; break; }
           }
         }
-        if (alive && nck > 0) final_state(1.f / c, (nck - 1) & 1);
       } else {
         for (int i = 0; i < nck && alive; ++i) {
           if (!kq_pass(i)) { alive = false; break; }
           if (!snapshot(i, 0, pw[chunk_len(i)])) { alive = false; break; }
         }
-        if (alive && nck > 0) final_state(1.f, (nck - 1) & 1);
       }
     }
+    if (et == 0) *reinterpret_cast<float*>(sm + L::oCState) = c;
   } else if (!SO) {
     // ================= output group (warps 6..9) =================
     const int eo = threadIdx.x - 192;
@@ -731,14 +853,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       if (!go(L::bPFull + pb, (j / NP) & 1)) return false;
       tc_fence_after();
       const uint32_t tP = tmem + lane_addr + L::cP + pb * C;
-#pragma unroll 1
-      for (int cb = 0; cb < C / 32; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tP + cb * 32, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
+      for (int cb = 0; cb < C / 32; cb += 2) {
+        uint32_t r[64];
+        tmem_ld32p(tP + cb * 32, &r[0]);
+        tmem_ld32p(tP + cb * 32 + 32, &r[32]);
+        tmem_wait_ld();
+        uint32_t pk[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
           const int c0 = cb * 32 + 2 * jj;
           float a = __uint_as_float(r[2 * jj]), b = __uint_as_float(r[2 * jj + 1]);
           if (fast) {
@@ -750,7 +873,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           }
           pk[jj] = pack_bf16(a, b);
         }
-        tmem_st16(tP + cb * 16, pk);
+        // P~ columns 16*cb .. 16*cb+31 lie in P columns already read
+        tmem_st16(tP + cb * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tP + cb * 16 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
       }
       tmem_wait_st();
       tc_fence_before();
@@ -766,32 +891,40 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       float rt = 0.f;
       if (arow >= 0 && arow < len) rt = fast ? p.scale / (ci * pw[len - 1 - arow]) : 1.f;
       const int vs = i % NV;
-      uint8_t* stg = sm + L::oV + vs * L::kV;
+      uint8_t* stg = L::kSepStage ? sm + L::oStg : sm + L::oV + vs * L::kV;
       const uint32_t tO = tmem + lane_addr + L::cO + ob * DVT;
-#pragma unroll 1
-      for (int cb = 0; cb < DVT / 32; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tO + cb * 32, r);
-        tmem_wait_ld();
-        if (arow >= 0) {
-          uint32_t pk[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            pk[jj] = pack_bf16(rt * __uint_as_float(r[2 * jj]), rt * __uint_as_float(r[2 * jj + 1]));
-          store_row32_packed(stg, C, arow, cb * 32, pk);
+      for (int cb = 0; cb < DVT / 32; cb += 2) {
+        uint32_t r[64];
+        tmem_ld32p(tO + cb * 32, &r[0]);
+        tmem_ld32p(tO + cb * 32 + 32, &r[32]);
+        tmem_wait_ld();
+        if (cb + 2 >= DVT / 32) {
+          tc_fence_before();
+          mbar_arrive(bar(L::bOFree + ob));  // the next product may overwrite O now
+        }
+        // the staging buffer is free once the previous store has read it (the
+        // thread that issued that store waited for this before the barrier)
+        if (L::kSepStage && cb == 0) named_bar_sync(kBarO, kGroup);
+        if (arow >= 0) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            pk[j] = pack_bf16(rt * __uint_as_float(r[2 * j]), rt * __uint_as_float(r[2 * j + 1]));
+          store_row32_packed(stg, C, arow, cb * 32, &pk[0]);
+          store_row32_packed(stg, C, arow, cb * 32 + 32, &pk[16]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(L::bOFree + ob));
       fence_proxy_async_smem();
       named_bar_sync(kBarO, kGroup);
       if (eo == 0) {
         const int row0 = (c_begin + i) * C;
 #pragma unroll
-        for (int b = 0; b < DVT / 64; ++b) tma_store_3d(&tmo, v_slot(vs) + b * C * 128, dv0 + b * 64, row0, bh);
+        for (int b = 0; b < DVT / 64; ++b)
+          tma_store_3d(&tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, row0, bh);
         bulk_commit_group();
-        bulk_wait_group_read0();  // the slot may be refilled once the store has read it
-        mbar_arrive(bar(L::bVEmpty + vs));
+        bulk_wait_group_read0();  // the buffer may be rewritten once the store has read it
+        if (!L::kSepStage) mbar_arrive(bar(L::bVEmpty + vs));
       }
       return true;
     };
@@ -803,20 +936,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       if (nck > 0) alive = ptilde(0);
       for (int i = 0; i < nck && alive; ++i) {
         if (i + 1 < nck && !ptilde(i + 1)) { alive = false; break; }
-        frame_advance(c, n, pw[chunk_len(i)]);
+        frame_advance(c, n, inv_g(i));
         if (!out_chunk(i, c)) { alive = false; break; }
       }
     } else {
       for (int i = 0; i < nck && alive; ++i) {
         if (!ptilde(i)) { alive = false; break; }
-        if (fast) frame_advance(c, n, pw[chunk_len(i)]);
+        if (fast) frame_advance(c, n, inv_g(i));
         if (!out_chunk(i, c)) { alive = false; break; }
       }
     }
     if (eo == 0) bulk_wait_group0();
   }
 
-  // ---- teardown ----
+  // ---- teardown: every MMA has completed, every load landed, every store read ----
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  write_final_state<C, DK, DVT, SO>(p, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
