@@ -122,7 +122,7 @@ struct Cfg {
   static constexpr int NQK = pick_nqk();
   static constexpr int pick_nv() {
     int v = NQK;
-    while (v < 8 && bytes(NQK, v + 1, NSB, NSTG) <= kMaxSmemPerBlock) ++v;
+    while (!(SO && H == 1) && v < 8 && bytes(NQK, v + 1, NSB, NSTG) <= kMaxSmemPerBlock) ++v;
     return v;
   }
   static constexpr int NV = pick_nv();
@@ -152,7 +152,14 @@ struct Cfg {
   // both chunks' Q/K halves and P buffers fit at once and the V ring (whose
   // slots also stage the outputs) is deep enough that chunk i+1's loads do not
   // wait for the store of chunk i-1.
-  static constexpr bool kLookahead = !SO && NQK >= 2 * H && NP >= 2 && NV >= 3;
+  static constexpr bool kLookahead = !SO && NQK >= 2 * H && NP >= 2 && NO >= 2 && NV >= 3;
+  // Completions that coincide share one barrier: P-buffer reuse and (with two
+  // or more single-half snapshot buffers) snapshot reuse wait for the output
+  // barrier of the chunk that last used the buffer, which implies both.
+  static constexpr bool kMergePFree = NP == NO;
+  static constexpr bool kMergeSbFree = H == 1 && NSB >= 2 && NSB == NO;
+  // State-only pass: one release per chunk frees its K and V slots together.
+  static constexpr bool kUnifiedStage = SO && H == 1 && NQK == NV;
   // barriers
   static constexpr int bQkFull = 0, bQkEmpty = NQK, bVFull = 2 * NQK, bVEmpty = 2 * NQK + NV,
                        bWReady = 2 * NQK + 2 * NV, bSRead = 2 * NQK + 3 * NV, bSFull = bSRead + H,
@@ -338,28 +345,34 @@ __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, u
   }
 }
 
-template <int C, int DK, int DVT, bool SO>
-__global__ void __launch_bounds__(kThreads, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
-                const TcParams p) {
+// What the roles of one CTA share, set up by the kernel before they start.
+struct RoleCtx {
+  const CUtensorMap *tmq, *tmk, *tmv, *tmo;
+  uint8_t* sm;
+  uint32_t tmem;
+  float inv_gC;  // 1 / gamma^C (rescaled form only)
+};
+
+// The four roles of a CTA (producer, MMA issuer, state group, output group).
+// FAST selects the rescaled form; a CTA picks one instantiation at its start,
+// so the code it runs holds no branches of the other form.
+template <int C, int DK, int DVT, bool SO, bool FAST>
+__device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x) {
   using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
-  extern __shared__ uint8_t smem_raw[];
-  // Align by pointer arithmetic on the __shared__ array itself (not through an
-  // integer), so the compiler keeps every access below in the shared window.
-  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr bool fast = FAST;
+  constexpr bool look = L::kLookahead;
+  uint8_t* sm = x.sm;
   const uint32_t sbase = smem_u32(sm);
-  float* pw = reinterpret_cast<float*>(sm + L::oPw);  // pw[d] = gamma^d, d = 0..C
+  const uint32_t tmem = x.tmem;
+  const float inv_gC = x.inv_gC;
+  float* pw = reinterpret_cast<float*>(sm + L::oPw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oAbort);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oSlot);
   auto bar = [&](int i) { return sbase + L::oBar + 8 * i; };
   auto qk_q = [&](int s) { return sbase + s * L::kQK; };
   auto qk_k = [&](int s) { return sbase + s * L::kQK + L::kQ; };
   auto v_slot = [&](int s) { return sbase + L::oV + s * L::kV; };
   auto sb_buf = [&](int b) { return sbase + L::oSb + b * L::kSb; };
-
-  // ---- work item: (dv tile fastest, then head, then segment) ----
   int idx = blockIdx.x;
   const int dvt = idx % p.n_dv_tiles;
   idx /= p.n_dv_tiles;
@@ -371,9 +384,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   const int dv0 = dvt * DVT;
   const float g = p.gamma[head];
   const float lg = g > 0.f ? log2f(g) : 0.f;
-  const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
   const bool zero_init = SO || seg == 0;
-  const bool look = L::kLookahead && fast;
   auto chunk_len = [&](int i) { return min(C, p.N - (c_begin + i) * C); };
   // Segment states in the workspace are stored lane-major: float4 number
   // (c4 * 128 + row) of block (bh, segment, dv tile, half) holds columns
@@ -382,64 +393,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     return reinterpret_cast<float4*>(p.ws) +
            ((((size_t)bh * (p.segments - 1) + s) * p.n_dv_tiles + dvt) * H + hh) * (size_t)(DVT / 4) * 128;
   };
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float inv_gC = 1.f;   // 1 / gamma^C (rescaled form only), set once pw[] is filled
   auto inv_g = [&](int i) {
     const int len = chunk_len(i);
     return len == C ? inv_gC : 1.f / pw[len];
   };
-
-  // ---- set-up ----
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NQK; ++i) {
-      mbar_init(bar(L::bQkFull + i), 1);
-      mbar_init(bar(L::bQkEmpty + i), 1);
-    }
-    for (int i = 0; i < NV; ++i) {
-      mbar_init(bar(L::bVFull + i), 1);
-      mbar_init(bar(L::bVEmpty + i), 1);
-      mbar_init(bar(L::bWReady + i), kGroup);
-    }
-    for (int i = 0; i < H; ++i) {
-      mbar_init(bar(L::bSRead + i), kGroup);
-      mbar_init(bar(L::bSFull + i), 1);
-    }
-    for (int i = 0; i < NSB; ++i) {
-      mbar_init(bar(L::bSbReady + i), kGroup);
-      mbar_init(bar(L::bSbFree + i), 1);
-    }
-    for (int i = 0; i < NP; ++i) {
-      mbar_init(bar(L::bPFull + i), 1);
-      mbar_init(bar(L::bPFree + i), 1);
-      mbar_init(bar(L::bPtReady + i), kGroup);
-    }
-    for (int i = 0; i < NO; ++i) {
-      mbar_init(bar(L::bOFull + i), 1);
-      mbar_init(bar(L::bOFree + i), kGroup);
-    }
-    mbar_init(bar(L::bFin), 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-    if (!SO) prefetch_tensormap(&tmq);
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-    if (!SO) prefetch_tensormap(&tmo);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
-    tmem_relinquish();
-  }
-  for (int d = threadIdx.x; d <= C; d += kThreads) pw[d] = gamma_pow(g, lg, (float)d);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  if (fast) inv_gC = 1.f / pw[C];
-  // The main pass may start its CTAs now.  This comes after the TMEM
-  // allocation, so a main-pass CTA that lands on this SM and waits for this
-  // grid can never hold the columns this CTA still needs.
-  if (SO) griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -457,12 +415,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           mbar_arrive_expect_tx(bar(L::bVFull + s), L::kV);
 #pragma unroll
           for (int b = 0; b < DVT / 64; ++b)
-            tma_load_3d(v_slot(s) + b * C * 128, &tmv, dv0 + b * 64, row, bh, bar(L::bVFull + s));
+            tma_load_3d(v_slot(s) + b * C * 128, x.tmv, dv0 + b * 64, row, bh, bar(L::bVFull + s));
           v_issued = i + 1;
         }
         for (int hh = 0; hh < H; ++hh) {
           const int u = i * H + hh, s = u % NQK, k = u / NQK;
-          if (k > 0 && !wait_bar(bar(L::bQkEmpty + s), (k - 1) & 1, abort_flag)) {
+          if (!L::kUnifiedStage && k > 0 && !wait_bar(bar(L::bQkEmpty + s), (k - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -470,11 +428,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           if (!SO) {
 #pragma unroll
             for (int b = 0; b < 2; ++b)
-              tma_load_3d(qk_q(s) + b * C * 128, &tmq, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
+              tma_load_3d(qk_q(s) + b * C * 128, x.tmq, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
           }
 #pragma unroll
           for (int b = 0; b < 2; ++b)
-            tma_load_3d(qk_k(s) + b * C * 128, &tmk, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
+            tma_load_3d(qk_k(s) + b * C * 128, x.tmk, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
           qk_issued = u + 1;
         }
       }
@@ -490,7 +448,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       constexpr uint32_t idP = make_idesc(C, C, false, false);
       constexpr uint32_t idO = make_idesc(C, DVT, false, true);
       constexpr uint32_t idS = make_idesc(128, DVT, true, true);
-      auto test = [&](int b, int parity) { return mbar_test_wait(bar(b), (uint32_t)(parity & 1)); };
       auto has_state = [&](int i) { return i > 0 || !zero_init; };
       // S_h = 2^-n S_h + K_h^T W  (or S_h = K_h^T W when the state is zero)
       auto mma_s = [&](int i, int hh, int n) {
@@ -530,119 +487,102 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             tc_fence_after();
             mma_s(i, hh, n);
             if (!fast) mma_commit(bar(L::bSFull + hh));
-            mma_commit(bar(L::bQkEmpty + u % NQK));
+            if (!L::kUnifiedStage) mma_commit(bar(L::bQkEmpty + u % NQK));
           }
           if (ok) mma_commit(bar(L::bVEmpty + vs));
         }
       } else {
-        // Four in-order streams, each MMA issued as soon as its operands are
-        // ready, by priority: the state chain, Q S (it frees the snapshot
-        // buffer and the Q/K slot), Q K^T, P~ W.
+        // Static issue order, chosen so that each wait is normally met by
+        // work issued an iteration earlier.  With lookahead (chunk i+1's Q K^T
+        // may run while chunk i still holds its P buffer), chunk i issues
+        //   S(i), Q S(i), P~ W(i-1), Q K^T(i+1);
+        // without, Q K^T(i), S(i), Q S(i), P~ W(i).  S and Q S go half by
+        // half, since with one snapshot buffer the copy of half 1 waits for
+        // the Q S product of half 0.
         float c = 1.f;
-        int n = 0;
-        int qk_ok = 0;                      // Q/K units known to be loaded
-        int s_i = 0, s_h = 0;               // next state update
-        bool s_w = false;                   // its W (or K^/Q~) is ready
-        int p_j = 0;                        // next Q K^T
-        int oi_i = 0, oi_h = 0;             // next Q S
-        int oa_i = 0;                       // next P~ W
-        auto qk_ready = [&](int u_end) {
-          while (qk_ok < u_end) {
-            if (!test(L::bQkFull + qk_ok % NQK, qk_ok / NQK)) return false;
-            ++qk_ok;
+        int n = 0, qk_waited = 0;
+        auto wait = [&](int b, int par) { return wait_bar(bar(b), (uint32_t)(par & 1), abort_flag); };
+        auto wait_qk = [&](int u_end) -> bool {
+          while (qk_waited < u_end) {
+            if (!wait(L::bQkFull + qk_waited % NQK, qk_waited / NQK)) return false;
+            ++qk_waited;
           }
           return true;
         };
-        uint64_t t_last = globaltimer_ns();
-        while (oa_i < nck) {
-          bool issued = false;
-          if (s_i < nck) {
-            const int vs = s_i % NV;
-            if (!s_w)
-              s_w = test(L::bWReady + vs, s_i / NV) && (fast || test(L::bVFull + vs, s_i / NV));
-            if (s_w && qk_ready(s_i * H + s_h + 1) && test(L::bSRead + s_h, s_i)) {
-              tc_fence_after();
-              if (s_h == 0 && fast) frame_advance(c, n, inv_g(s_i));
-              mma_s(s_i, s_h, fast ? n : 0);
-              mma_commit(bar(L::bSFull + s_h));
-              if (++s_h == H) {
-                s_h = 0;
-                ++s_i;
-                s_w = false;
-              }
-              issued = true;
-            }
-          }
-          if (!issued && (oi_i < s_i || (oi_i == s_i && oi_h < s_h)) && oi_i < p_j) {
-            // O (+)= Q_h Sb_h once the state update of half h is issued (the
-            // snapshot of the next half may wait for this product to free the
-            // buffer); afterwards the chunk's Q/K half is no longer read
-            const int ob = oi_i % NO, ko = oi_i / NO;
-            const int u = oi_i * H + oi_h, b = u % NSB;
-            if ((oi_h > 0 || ko == 0 || test(L::bOFree + ob, ko - 1)) && test(L::bSbReady + b, u / NSB)) {
-              tc_fence_after();
-              if (has_state(oi_i)) {
-                const int s = u % NQK;
+        // P[j % NP] = Q_j K_j^T
+        auto issue_p = [&](int j) -> bool {
+          const int pb = j % NP;
+          if (j >= NP && !wait(L::kMergePFree ? L::bOFull + pb : L::bPFree + pb, j / NP - 1)) return false;
+          if (!wait_qk((j + 1) * H)) return false;
+          tc_fence_after();
+          for (int hh = 0; hh < H; ++hh) {
+            const int s = (j * H + hh) % NQK;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                  const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
-                  mma_bf16(tmem + L::cO + ob * DVT, make_sdesc(qk_q(s) + aoff, 16, 1024),
-                           make_sdesc(sb_buf(b) + kk * 2048, 128 * 128, 1024), idO,
-                           (oi_h > 0 || kk > 0) ? 1u : 0u);
-                }
-              }
-              mma_commit(bar(L::bSbFree + b));
-              mma_commit(bar(L::bQkEmpty + u % NQK));
-              if (++oi_h == H) {
-                oi_h = 0;
-                ++oi_i;
-              }
-              issued = true;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk / 4) * C * 128 + (kk % 4) * 32;
+              mma_bf16(tmem + L::cP + pb * C, make_sdesc(qk_q(s) + off, 16, 1024),
+                       make_sdesc(qk_k(s) + off, 16, 1024), idP, (hh > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          if (!issued && p_j < nck && qk_ready((p_j + 1) * H) &&
-              (p_j < NP || test(L::bPFree + p_j % NP, p_j / NP - 1))) {
-            // P[j % NP] = Q_j K_j^T
-            tc_fence_after();
-            const int pb = p_j % NP;
-            for (int hh = 0; hh < H; ++hh) {
-              const int s = (p_j * H + hh) % NQK;
+          mma_commit(bar(L::bPFull + pb));
+          return true;
+        };
+        // state update of half hh, then O (+)= Q_hh Sb_hh
+        auto issue_s_qs = [&](int i, int hh) -> bool {
+          const int vs = i % NV, ob = i % NO, u = i * H + hh, b = u % NSB;
+          if (hh == 0) {
+            if (!wait(L::bWReady + vs, i / NV)) return false;
+            if (!fast && !wait(L::bVFull + vs, i / NV)) return false;
+            if (fast) frame_advance(c, n, inv_g(i));
+          }
+          if (!wait_qk(u + 1) || !wait(L::bSRead + hh, i)) return false;
+          tc_fence_after();
+          mma_s(i, hh, fast ? n : 0);
+          mma_commit(bar(L::bSFull + hh));
+          if (hh == 0 && i >= NO && !wait(L::bOFree + ob, i / NO - 1)) return false;
+          if (!wait(L::bSbReady + b, u / NSB)) return false;
+          tc_fence_after();
+          if (has_state(i)) {
+            const int s = u % NQK;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk / 4) * C * 128 + (kk % 4) * 32;
-                mma_bf16(tmem + L::cP + pb * C, make_sdesc(qk_q(s) + off, 16, 1024),
-                         make_sdesc(qk_k(s) + off, 16, 1024), idP, (hh > 0 || kk > 0) ? 1u : 0u);
-              }
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
+              mma_bf16(tmem + L::cO + ob * DVT, make_sdesc(qk_q(s) + aoff, 16, 1024),
+                       make_sdesc(sb_buf(b) + kk * 2048, 128 * 128, 1024), idO, (hh > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(bar(L::bPFull + pb));
-            ++p_j;
-            issued = true;
           }
-          if (!issued && oa_i < oi_i && test(L::bPtReady + oa_i % NP, oa_i / NP)) {
-            // O += P~ W, P~ read from tensor memory
-            tc_fence_after();
-            const int ob = oa_i % NO, pb = oa_i % NP, vs = oa_i % NV;
+          if (!L::kMergeSbFree) mma_commit(bar(L::bSbFree + b));
+          mma_commit(bar(L::bQkEmpty + u % NQK));  // the chunk's Q/K half is no longer read
+          return true;
+        };
+        // O += P~ W, P~ read from tensor memory
+        auto issue_pw = [&](int i) -> bool {
+          const int ob = i % NO, pb = i % NP, vs = i % NV;
+          if (!wait(L::bPtReady + pb, i / NP)) return false;
+          tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < C / 16; ++kk)
-              mma_bf16_ta(tmem + L::cO + ob * DVT, tmem + L::cP + pb * C + kk * 8,
-                          make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024), idO,
-                          (has_state(oa_i) || kk > 0) ? 1u : 0u);
-            mma_commit(bar(L::bOFull + ob));
-            mma_commit(bar(L::bPFree + pb));
-            if (L::kSepStage) mma_commit(bar(L::bVEmpty + vs));  // V slot free once the MMAs are done
-            ++oa_i;
-            issued = true;
+          for (int kk = 0; kk < C / 16; ++kk)
+            mma_bf16_ta(tmem + L::cO + ob * DVT, tmem + L::cP + pb * C + kk * 8,
+                        make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024), idO, (has_state(i) || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::bOFull + ob));
+          if (!L::kMergePFree) mma_commit(bar(L::bPFree + pb));
+          if (L::kSepStage) mma_commit(bar(L::bVEmpty + vs));  // V slot free once the MMAs are done
+          return true;
+        };
+        auto issue_s_all = [&](int i) -> bool {
+          for (int hh = 0; hh < H; ++hh)
+            if (!issue_s_qs(i, hh)) return false;
+          return true;
+        };
+        // one call site per step keeps the issuer's code small
+        if (look) {
+          for (int i = -1; i <= nck && ok; ++i) {
+            if (i >= 0 && i < nck) ok = issue_s_all(i);
+            if (ok && i >= 1) ok = issue_pw(i - 1);
+            if (ok && i + 1 < nck) ok = issue_p(i + 1);
           }
-          if (issued) {
-            t_last = globaltimer_ns();
-          } else {
-            nanosleep_ns(32);  // leave the issue slots to the epilogue warps
-            if (*abort_flag) break;
-            if (globaltimer_ns() - t_last > kWaitLimitNs) {
-              flag_timeout(abort_flag);
-              break;
-            }
-          }
+        } else {
+          for (int i = 0; i < nck && ok; ++i) ok = issue_p(i) && issue_s_all(i) && issue_pw(i);
         }
       }
       // every issued MMA has completed before TMEM is released
@@ -733,7 +673,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         const uint32_t tS = tmem + lane_addr + L::cS + hh * DVT;
         const int u = i * H + hh, b = u % NSB;
         uint8_t* sb = sm + L::oSb + b * L::kSb;
-        if (u >= NSB && !gw(L::bSbFree + b, (u / NSB - 1) & 1)) return false;
+        if (u >= NSB && !gw(L::kMergeSbFree ? L::bOFull + b : L::bSbFree + b, (u / NSB - 1) & 1)) return false;
         if (has_state && i > 0 && !gw(L::bSFull + hh, (i - 1) & 1)) return false;
         if (has_state) {
           tc_fence_after();
@@ -817,14 +757,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       if (fast) {
         float c_next = 1.f;
         int n_next = 0;
-        if (nck > 0) {
-          frame_advance(c_next, n_next, inv_g(0));
-          alive = w_pass(0, c_next);
-        }
-        for (int i = 0; i < nck && alive; ++i) {
-          c = c_next;
-          n = n_next;
-          if (!snapshot(i, n, 1.f)) { alive = false; break; }
+        for (int i = -1; i < nck && alive; ++i) {
+          if (i >= 0) {
+            c = c_next;
+            n = n_next;
+            if (!snapshot(i, n, 1.f)) { alive = false; break; }
+          }
           if (i + 1 < nck) {
             frame_advance(c_next, n_next, inv_g(i + 1));
             if (!w_pass(i + 1, c_next)) { alive = false; break; }
@@ -921,7 +859,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         const int row0 = (c_begin + i) * C;
 #pragma unroll
         for (int b = 0; b < DVT / 64; ++b)
-          tma_store_3d(&tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, row0, bh);
+          tma_store_3d(x.tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, row0, bh);
         bulk_commit_group();
         bulk_wait_group_read0();  // the buffer may be rewritten once the store has read it
         if (!L::kSepStage) mbar_arrive(bar(L::bVEmpty + vs));
@@ -933,10 +871,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     int n = 0;
     bool alive = true;
     if (look) {
-      if (nck > 0) alive = ptilde(0);
-      for (int i = 0; i < nck && alive; ++i) {
+      for (int i = -1; i < nck && alive; ++i) {
         if (i + 1 < nck && !ptilde(i + 1)) { alive = false; break; }
-        frame_advance(c, n, inv_g(i));
+        if (i < 0) continue;
+        if (fast) frame_advance(c, n, inv_g(i));
         if (!out_chunk(i, c)) { alive = false; break; }
       }
     } else {
@@ -948,6 +886,86 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     }
     if (eo == 0) bulk_wait_group0();
   }
+
+}
+
+template <int C, int DK, int DVT, bool SO>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                const TcParams p) {
+  using L = Cfg<C, DK, DVT, SO>;
+  constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
+  extern __shared__ uint8_t smem_raw[];
+  // Align by pointer arithmetic on the __shared__ array itself (not through an
+  // integer), so the compiler keeps every access below in the shared window.
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(sm);
+  float* pw = reinterpret_cast<float*>(sm + L::oPw);  // pw[d] = gamma^d, d = 0..C
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oSlot);
+  auto bar = [&](int i) { return sbase + L::oBar + 8 * i; };
+  const int head = (blockIdx.x / p.n_dv_tiles) % p.BH % p.H;
+  const float g = p.gamma[head];
+  const float lg = g > 0.f ? log2f(g) : 0.f;
+  const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
+  const int warp = threadIdx.x >> 5;
+  float inv_gC = 1.f;
+
+  // ---- set-up ----
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NQK; ++i) {
+      mbar_init(bar(L::bQkFull + i), 1);
+      mbar_init(bar(L::bQkEmpty + i), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(bar(L::bVFull + i), 1);
+      mbar_init(bar(L::bVEmpty + i), 1);
+      mbar_init(bar(L::bWReady + i), kGroup);
+    }
+    for (int i = 0; i < H; ++i) {
+      mbar_init(bar(L::bSRead + i), kGroup);
+      mbar_init(bar(L::bSFull + i), 1);
+    }
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(bar(L::bSbReady + i), kGroup);
+      mbar_init(bar(L::bSbFree + i), 1);
+    }
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(bar(L::bPFull + i), 1);
+      mbar_init(bar(L::bPFree + i), 1);
+      mbar_init(bar(L::bPtReady + i), kGroup);
+    }
+    for (int i = 0; i < NO; ++i) {
+      mbar_init(bar(L::bOFull + i), 1);
+      mbar_init(bar(L::bOFree + i), kGroup);
+    }
+    mbar_init(bar(L::bFin), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    if (!SO) prefetch_tensormap(&tmq);
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+    if (!SO) prefetch_tensormap(&tmo);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+  for (int d = threadIdx.x; d <= C; d += kThreads) pw[d] = gamma_pow(g, lg, (float)d);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (fast) inv_gC = 1.f / pw[C];
+  // The main pass may start its CTAs now.  This comes after the TMEM
+  // allocation, so a main-pass CTA that lands on this SM and waits for this
+  // grid can never hold the columns this CTA still needs.
+  if (SO) griddep_launch_dependents();
+
+  const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC};
+  if (fast) chunk_roles<C, DK, DVT, SO, true>(p, x);
+  else chunk_roles<C, DK, DVT, SO, false>(p, x);
 
   // ---- teardown: every MMA has completed, every load landed, every store read ----
   tc_fence_before();
