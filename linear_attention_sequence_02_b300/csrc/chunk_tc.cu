@@ -201,9 +201,8 @@ __device__ __forceinline__ void flag_timeout(volatile int* abort_flag) {
   atomicOr(&g_device_status, RET_DEV_WAIT_TIMEOUT);
 }
 
-// Wait for phase `parity` of `bar`; false if this CTA is aborting or the wait timed out.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The waiting loop of wait_bar.
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -213,6 +212,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       return false;
     }
   }
+}
+
+// Wait for phase `parity` of `bar`; false if this CTA is aborting or the wait timed out.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, abort_flag);
 }
 
 // Teardown wait: ignores the abort flag, still bounded.
@@ -256,13 +261,33 @@ __device__ __forceinline__ void store_row32_packed(uint8_t* tile, int rows_per_b
 // (ROWS rows per 64-column box, NBYTES in total) by f(r).  Each of the group's
 // threads loads a batch of up to eight 16-byte units before it scales and
 // stores any, so a batch costs about one shared-memory round trip.
+// Descriptor of `addr` + `bytes`: the start address sits in the low 14 bits of
+// a shared-memory descriptor in 16-byte units, and shared addresses stay below
+// 256 KB, so a byte offset is added to the descriptor directly.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+// Byte offset of K-step kk (16 elements) in a K-major, 128-byte-swizzled
+// operand of `rows` rows stored as 64-column boxes.
+__device__ __forceinline__ uint32_t kmajor_step(int kk, int rows) { return (kk >> 2) * rows * 128 + (kk & 3) * 32; }
+
+// D (+)= A B^T over `steps` K-steps of 16, operands from shared memory; a K-step
+// advances A by a_step(kk) and B by b_step(kk) bytes (descriptors are offset,
+// not rebuilt, per step).
+template <class FA, class FB>
+__device__ __forceinline__ void mma_run(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, int steps,
+                                        bool accumulate_first, FA a_step, FB b_step) {
+  mma_bf16(d, da, db, idesc, accumulate_first ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < steps; ++kk) mma_bf16(d, desc_add(da, a_step(kk)), desc_add(db, b_step(kk)), idesc, 1u);
+}
+
 template <int NBYTES, int ROWS, class F>
 __device__ __forceinline__ void scale_rows_bf16(uint8_t* base, int tid, F f) {
   static_assert(NBYTES % (16 * kGroup) == 0, "tile size");
   constexpr int kUnits = NBYTES / (16 * kGroup);
   constexpr int kBatch = kUnits < 8 ? kUnits : 8;  // at most 32 registers of data in flight
   static_assert(kUnits % kBatch == 0, "batch");
-#pragma unroll
+#pragma unroll 1
   for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
     uint4 v[kBatch];
 #pragma unroll
@@ -453,14 +478,11 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       auto mma_s = [&](int i, int hh, int n) {
         const int s = (i * H + hh) % NQK, vs = i % NV;
         const uint32_t d = tmem + L::cS + hh * DVT;
+        const uint64_t a = make_sdesc(qk_k(s), C * 128, 1024), b = make_sdesc(v_slot(vs), C * 128, 1024);
+        if (has_state(i)) mma_bf16_scaled(d, a, b, idS, n);
+        else mma_bf16(d, a, b, idS, 0u);
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk) {
-          const uint64_t a = make_sdesc(qk_k(s) + kk * 2048, C * 128, 1024);
-          const uint64_t b = make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024);
-          if (kk > 0) mma_bf16(d, a, b, idS, 1u);
-          else if (has_state(i)) mma_bf16_scaled(d, a, b, idS, n);
-          else mma_bf16(d, a, b, idS, 0u);
-        }
+        for (int kk = 1; kk < C / 16; ++kk) mma_bf16(d, desc_add(a, kk * 2048), desc_add(b, kk * 2048), idS, 1u);
       };
       bool ok = true;
       if (SO) {
@@ -515,14 +537,12 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           if (j >= NP && !wait(L::kMergePFree ? L::bOFull + pb : L::bPFree + pb, j / NP - 1)) return false;
           if (!wait_qk((j + 1) * H)) return false;
           tc_fence_after();
+#pragma unroll 1
           for (int hh = 0; hh < H; ++hh) {
             const int s = (j * H + hh) % NQK;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk / 4) * C * 128 + (kk % 4) * 32;
-              mma_bf16(tmem + L::cP + pb * C, make_sdesc(qk_q(s) + off, 16, 1024),
-                       make_sdesc(qk_k(s) + off, 16, 1024), idP, (hh > 0 || kk > 0) ? 1u : 0u);
-            }
+            auto kstep = [](int kk) { return kmajor_step(kk, C); };
+            mma_run(tmem + L::cP + pb * C, make_sdesc(qk_q(s), 16, 1024), make_sdesc(qk_k(s), 16, 1024), idP, 8,
+                    hh > 0, kstep, kstep);
           }
           mma_commit(bar(L::bPFull + pb));
           return true;
@@ -544,12 +564,8 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           tc_fence_after();
           if (has_state(i)) {
             const int s = u % NQK;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t aoff = (kk / 4) * C * 128 + (kk % 4) * 32;
-              mma_bf16(tmem + L::cO + ob * DVT, make_sdesc(qk_q(s) + aoff, 16, 1024),
-                       make_sdesc(sb_buf(b) + kk * 2048, 128 * 128, 1024), idO, (hh > 0 || kk > 0) ? 1u : 0u);
-            }
+            mma_run(tmem + L::cO + ob * DVT, make_sdesc(qk_q(s), 16, 1024), make_sdesc(sb_buf(b), 128 * 128, 1024),
+                    idO, 8, hh > 0, [](int kk) { return kmajor_step(kk, C); }, [](int kk) { return (uint32_t)kk * 2048; });
           }
           if (!L::kMergeSbFree) mma_commit(bar(L::bSbFree + b));
           mma_commit(bar(L::bQkEmpty + u % NQK));  // the chunk's Q/K half is no longer read
@@ -560,10 +576,13 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           const int ob = i % NO, pb = i % NP, vs = i % NV;
           if (!wait(L::bPtReady + pb, i / NP)) return false;
           tc_fence_after();
+          {
+            const uint64_t db = make_sdesc(v_slot(vs), C * 128, 1024);
+            const uint32_t dO = tmem + L::cO + ob * DVT, aP = tmem + L::cP + pb * C;
+            mma_bf16_ta(dO, aP, db, idO, has_state(i) ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk)
-            mma_bf16_ta(tmem + L::cO + ob * DVT, tmem + L::cP + pb * C + kk * 8,
-                        make_sdesc(v_slot(vs) + kk * 2048, C * 128, 1024), idO, (has_state(i) || kk > 0) ? 1u : 0u);
+            for (int kk = 1; kk < C / 16; ++kk) mma_bf16_ta(dO, aP + kk * 8, desc_add(db, kk * 2048), idO, 1u);
+          }
           mma_commit(bar(L::bOFull + ob));
           if (!L::kMergePFree) mma_commit(bar(L::bPFree + pb));
           if (L::kSepStage) mma_commit(bar(L::bVEmpty + vs));  // V slot free once the MMAs are done
@@ -678,7 +697,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         if (has_state) {
           tc_fence_after();
           const float f = fast ? __uint_as_float((uint32_t)(127 - n) << 23) : 1.f;  // 2^-n
-#pragma unroll
+#pragma unroll 1
           for (int cb = 0; cb < DVT / 32; cb += 2) {
             uint32_t r[64];
             tmem_ld32p(tS + cb * 32, &r[0]);
@@ -791,7 +810,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       if (!go(L::bPFull + pb, (j / NP) & 1)) return false;
       tc_fence_after();
       const uint32_t tP = tmem + lane_addr + L::cP + pb * C;
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < C / 32; cb += 2) {
         uint32_t r[64];
         tmem_ld32p(tP + cb * 32, &r[0]);
@@ -831,7 +850,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       const int vs = i % NV;
       uint8_t* stg = L::kSepStage ? sm + L::oStg : sm + L::oV + vs * L::kV;
       const uint32_t tO = tmem + lane_addr + L::cO + ob * DVT;
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < DVT / 32; cb += 2) {
         uint32_t r[64];
         tmem_ld32p(tO + cb * 32, &r[0]);
