@@ -99,60 +99,98 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during a region."""
+    """SM clock and throttle reasons sampled during a region.
 
+    In-process NVML polling every millisecond (so even a region of a few
+    milliseconds gets several samples); if NVML is unavailable, nvidia-smi
+    every 200 ms.
+    """
+
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
+        self.samples = []  # (sm_mhz, max_mhz, set of reasons)
+        self._stop = threading.Event()
+        self._t = None
         self.proc = None
-        self.lines = []
+        self.source = None
 
     def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            mx = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            masks = [(name, getattr(pynvml, attr, getattr(pynvml, attr.replace("Event", "Throttle"), 0)))
+                     for name, attr in self.REASONS]
+
+            def poll():
+                while not self._stop.is_set():
+                    sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                    r = reasons(h)
+                    self.samples.append((float(sm), float(mx), {n for n, m in masks if r & m}))
+                    time.sleep(0.001)
+
+            self.source = "nvml 1 ms"
+            self._t = threading.Thread(target=poll, daemon=True)
+            self._t.start()
+            return self
+        except Exception:
+            pass
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi 200 ms"
+
+            def read():
+                names = [n for n, _ in self.REASONS]
+                for line in self.proc.stdout:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) < 6:
+                        continue
+                    try:
+                        self.samples.append((float(parts[0]), float(parts[1]),
+                                             {n for n, v in zip(names, parts[2:6]) if v.lower() == "active"}))
+                    except ValueError:
+                        continue
+
+            self._t = threading.Thread(target=read, daemon=True)
             self._t.start()
         except OSError:
             self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self._t:
+            self._t.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 6:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[2:6]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        reasons = set()
+        for _, _, r in self.samples:
+            reasons |= r
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
+                "sm_max_mhz": max(x[1] for x in self.samples),
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": self.source}
 
 
 def dist_setup():
@@ -185,7 +223,13 @@ def max_over_ranks(x: float, world: int, device) -> float:
 # our arm
 
 def time_chunkwise(w, steps, warmup, dev, flush, seed=0):
-    """Per-call CUDA-event times (ms) of retention_chunkwise, L2 flushed between calls."""
+    """Per-call device times (ms) of retention_chunkwise, L2 flushed between calls.
+
+    The call (state-only pre-pass, main pass launched with programmatic
+    dependent launch, stream-ordered scratch) is captured once in a CUDA graph
+    and each timed step replays it, so host-side launch work stays outside the
+    device-timed region.  Falls back to eager calls if capture is refused.
+    """
     from linear_attention_sequence_02_b300 import binding, inputs
     B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
     q, k, v = (x.to(dev) for x in inputs.qkv(B, H, N, dk, dv, seed, torch.bfloat16))
@@ -193,23 +237,43 @@ def time_chunkwise(w, steps, warmup, dev, flush, seed=0):
     out = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
     st = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(warmup):
+    for _ in range(max(1, warmup)):
         flush.zero_()
         binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
     torch.cuda.synchronize(dev)
-    times = []
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st,
+                                        stream=torch.cuda.current_stream(dev))
+        for _ in range(warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize(dev)
+    except Exception:
+        graph = None
+        torch.cuda.synchronize(dev)
+
+    def run():
+        if graph is not None:
+            graph.replay()
+        else:
+            binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
+
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for a, b in evs:
         flush.zero_()
         a.record(stream)
-        binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
+        run()
         b.record(stream)
     torch.cuda.synchronize(dev)
     times = [a.elapsed_time(b) for a, b in evs]
     launches = binding.chunkwise_launches(B, H, N, dk, dv, C) * steps
-    del q, k, v, out, st
-    return times, launches
+    how = "cuda graph replay" if graph is not None else "eager calls"
+    del graph, q, k, v, out, st
+    return times, launches, how
 
 
 def time_e2e(w, steps, warmup, dev, seed=0):
@@ -315,7 +379,7 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        times, launches = time_chunkwise(w, args.steps, args.warmup, dev, flush)
+        times, launches, how = time_chunkwise(w, args.steps, args.warmup, dev, flush)
     torch.cuda.synchronize(dev)
     barrier(world)
     total_ms = max_over_ranks(sum(times), world, dev)
@@ -357,7 +421,7 @@ def run_ours(args):
             "gpu_launches": DECODE["T"] * 3,
         }
         for wl in (LONG, B7):
-            t, n = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
+            t, n, _ = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
             a_s = statistics.median(t) / 1e3
             ach = chunk_bytes(wl) / a_s / 1e9
             extra[wl["name"]] = {
@@ -376,7 +440,8 @@ def run_ours(args):
         "config": {"workload": "mid retention chunkwise fwd", "B": w["B"], "H": w["H"], "N": w["N"],
                    "dk": w["dk"], "dv": w["dv"], "chunk": w["chunk"], "global_batch": w["B"] * world,
                    "seq_len": w["N"], "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": "flushed (512 MiB write) between timed steps"},
+                   "l2": "flushed (512 MiB write) between timed steps",
+                   "timing": how},
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -438,8 +503,8 @@ def run_only(args):
         return
     w = {"mid": MID, "long": LONG, "7b": B7}[args.only]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    t, n = time_chunkwise(w, args.steps, args.warmup, dev, flush)
-    print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": n}))
+    t, n, how = time_chunkwise(w, args.steps, args.warmup, dev, flush)
+    print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": n, "timing": how}))
 
 
 def main():
