@@ -216,7 +216,7 @@ __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, vol
 
 // Wait for phase `parity` of `bar`; false if this CTA is aborting or the wait timed out.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;  // cheap check first (no suspend)
   return wait_bar_slow(bar, parity, abort_flag);
 }
 
@@ -257,10 +257,19 @@ __device__ __forceinline__ void store_row32_packed(uint8_t* tile, int rows_per_b
         make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
 }
 
-// Multiply, in place, every bf16 element of row r of a tile of 128-byte rows
-// (ROWS rows per 64-column box, NBYTES in total) by f(r).  Each of the group's
-// threads loads a batch of up to eight 16-byte units before it scales and
-// stores any, so a batch costs about one shared-memory round trip.
+// Slot and phase parity of the next use of an N-slot ring, advanced by one.
+template <int N>
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == N) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // Descriptor of `addr` + `bytes`: the start address sits in the low 14 bits of
 // a shared-memory descriptor in 16-byte units, and shared addresses stay below
 // 256 KB, so a byte offset is added to the descriptor directly.
@@ -281,6 +290,10 @@ __device__ __forceinline__ void mma_run(uint32_t d, uint64_t da, uint64_t db, ui
   for (int kk = 1; kk < steps; ++kk) mma_bf16(d, desc_add(da, a_step(kk)), desc_add(db, b_step(kk)), idesc, 1u);
 }
 
+// Multiply, in place, every bf16 element of row r of a tile of 128-byte rows
+// (ROWS rows per 64-column box, NBYTES in total) by f(r).  Each of the group's
+// threads loads a batch of up to eight 16-byte units before it scales and
+// stores any, so a batch costs about one shared-memory round trip.
 template <int NBYTES, int ROWS, class F>
 __device__ __forceinline__ void scale_rows_bf16(uint8_t* base, int tid, F f) {
   static_assert(NBYTES % (16 * kGroup) == 0, "tile size");
@@ -469,49 +482,69 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
+    // One thread issues every MMA.  Its loop is a chain of dependent
+    // instructions with nothing on its SMSP to hide their latency, so ring
+    // slots and parities are running counters (no division) and operand
+    // descriptors are a per-ring base plus slot stride.
     if (lane == 0) {
       constexpr uint32_t idP = make_idesc(C, C, false, false);
       constexpr uint32_t idO = make_idesc(C, DVT, false, true);
       constexpr uint32_t idS = make_idesc(128, DVT, true, true);
-      auto has_state = [&](int i) { return i > 0 || !zero_init; };
-      // S_h = 2^-n S_h + K_h^T W  (or S_h = K_h^T W when the state is zero)
-      auto mma_s = [&](int i, int hh, int n) {
-        const int s = (i * H + hh) % NQK, vs = i % NV;
-        const uint32_t d = tmem + L::cS + hh * DVT;
-        const uint64_t a = make_sdesc(qk_k(s), C * 128, 1024), b = make_sdesc(v_slot(vs), C * 128, 1024);
-        if (has_state(i)) mma_bf16_scaled(d, a, b, idS, n);
+      constexpr uint32_t kQKs = L::kQK >> 4, kVs = L::kV >> 4, kSbs = L::kSb >> 4;  // slot strides
+      const uint64_t dQ = make_sdesc(qk_q(0), 16, 1024);          // Q, K-major A (Q K^T, Q S)
+      const uint64_t dKb = make_sdesc(qk_k(0), 16, 1024);         // K, K-major B (Q K^T)
+      const uint64_t dKa = make_sdesc(qk_k(0), C * 128, 1024);    // K^T, MN-major A (state)
+      const uint64_t dV = make_sdesc(v_slot(0), C * 128, 1024);   // W or V, MN-major B
+      const uint64_t dSb = make_sdesc(sb_buf(0), 128 * 128, 1024);  // snapshot, MN-major B
+      const uint32_t bQkFull = bar(L::bQkFull), bQkEmpty = bar(L::bQkEmpty), bVFull = bar(L::bVFull),
+                     bVEmpty = bar(L::bVEmpty), bWReady = bar(L::bWReady), bSRead = bar(L::bSRead),
+                     bSFull = bar(L::bSFull), bSbReady = bar(L::bSbReady), bSbFree = bar(L::bSbFree),
+                     bPFull = bar(L::bPFull), bPFree = bar(L::kMergePFree ? L::bOFull : L::bPFree),
+                     bPtReady = bar(L::bPtReady), bOFull = bar(L::bOFull), bOFree = bar(L::bOFree);
+      auto wait = [&](uint32_t b, uint32_t par) { return wait_bar(b, par & 1u, abort_flag); };
+      // state update of one half: S_h = 2^-n S_h + K_h^T W (S_h = K_h^T W when the state is zero)
+      auto mma_s = [&](uint32_t d, int qslot, int vslot, bool has_state, int n) {
+        const uint64_t a = dKa + (uint64_t)qslot * kQKs, b = dV + (uint64_t)vslot * kVs;
+        if (has_state) mma_bf16_scaled(d, a, b, idS, n);
         else mma_bf16(d, a, b, idS, 0u);
 #pragma unroll
-        for (int kk = 1; kk < C / 16; ++kk) mma_bf16(d, desc_add(a, kk * 2048), desc_add(b, kk * 2048), idS, 1u);
+        for (int kk = 1; kk < C / 16; ++kk) mma_bf16(d, a + kk * 128, b + kk * 128, idS, 1u);
       };
       bool ok = true;
+      float c = 1.f;
+      int n = 0;
+      RingPos<NQK> qk_w;  // next Q/K unit to wait for
+      int qk_waited = 0;
+      auto wait_qk = [&](int u_end) -> bool {
+        while (qk_waited < u_end) {
+          if (!wait(bQkFull + 8 * qk_w.slot, qk_w.phase)) return false;
+          qk_w.next();
+          ++qk_waited;
+        }
+        return true;
+      };
       if (SO) {
         // state only: S in chunk order, each once its W (or K^) and, in the
         // direct form, the decayed state are ready
-        float c = 1.f;
-        int n = 0, qk_waited = 0;
+        RingPos<NV> v;
+        RingPos<NQK> qs;
         for (int i = 0; i < nck && ok; ++i) {
-          const int vs = i % NV;
           if (fast) frame_advance(c, n, inv_g(i));
-          if (!wait_bar(bar(L::bWReady + vs), (i / NV) & 1, abort_flag) ||
-              (!fast && !wait_bar(bar(L::bVFull + vs), (i / NV) & 1, abort_flag))) {
+          if (!wait(bWReady + 8 * v.slot, v.phase) || (!fast && !wait(bVFull + 8 * v.slot, v.phase))) {
             ok = false;
             break;
           }
           for (int hh = 0; hh < H && ok; ++hh) {
-            const int u = i * H + hh;
-            while (ok && qk_waited <= u) {
-              ok = wait_bar(bar(L::bQkFull + qk_waited % NQK), (qk_waited / NQK) & 1, abort_flag);
-              ++qk_waited;
-            }
-            if (ok && !fast) ok = wait_bar(bar(L::bSRead + hh), i & 1, abort_flag);
+            ok = wait_qk(i * H + hh + 1) && (fast || wait(bSRead + 8 * hh, (uint32_t)i));
             if (!ok) break;
             tc_fence_after();
-            mma_s(i, hh, n);
-            if (!fast) mma_commit(bar(L::bSFull + hh));
-            if (!L::kUnifiedStage) mma_commit(bar(L::bQkEmpty + u % NQK));
+            mma_s(tmem + L::cS + hh * DVT, qs.slot, v.slot, i > 0, n);
+            if (!fast) mma_commit(bSFull + 8 * hh);
+            if (!L::kUnifiedStage) mma_commit(bQkEmpty + 8 * qs.slot);
+            qs.next();
           }
-          if (ok) mma_commit(bar(L::bVEmpty + vs));
+          if (ok) mma_commit(bVEmpty + 8 * v.slot);
+          v.next();
         }
       } else {
         // Static issue order, chosen so that each wait is normally met by
@@ -521,71 +554,63 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         // without, Q K^T(i), S(i), Q S(i), P~ W(i).  S and Q S go half by
         // half, since with one snapshot buffer the copy of half 1 waits for
         // the Q S product of half 0.
-        float c = 1.f;
-        int n = 0, qk_waited = 0;
-        auto wait = [&](int b, int par) { return wait_bar(bar(b), (uint32_t)(par & 1), abort_flag); };
-        auto wait_qk = [&](int u_end) -> bool {
-          while (qk_waited < u_end) {
-            if (!wait(L::bQkFull + qk_waited % NQK, qk_waited / NQK)) return false;
-            ++qk_waited;
-          }
-          return true;
-        };
+        RingPos<NQK> q_p, q_s;  // Q/K slot of the next unit for Q K^T, and for S / Q S
+        RingPos<NV> v_s, v_w;   // V slot of the next chunk for S, and for P~ W
+        auto has_state = [&](int i) { return i > 0 || !zero_init; };
         // P[j % NP] = Q_j K_j^T
         auto issue_p = [&](int j) -> bool {
-          const int pb = j % NP;
-          if (j >= NP && !wait(L::kMergePFree ? L::bOFull + pb : L::bPFree + pb, j / NP - 1)) return false;
+          const int pb = j & (NP - 1);
+          if (j >= NP && !wait(bPFree + 8 * pb, (uint32_t)(j / NP - 1))) return false;
           if (!wait_qk((j + 1) * H)) return false;
           tc_fence_after();
 #pragma unroll 1
           for (int hh = 0; hh < H; ++hh) {
-            const int s = (j * H + hh) % NQK;
-            auto kstep = [](int kk) { return kmajor_step(kk, C); };
-            mma_run(tmem + L::cP + pb * C, make_sdesc(qk_q(s), 16, 1024), make_sdesc(qk_k(s), 16, 1024), idP, 8,
-                    hh > 0, kstep, kstep);
+            const uint64_t a = dQ + (uint64_t)q_p.slot * kQKs, b = dKb + (uint64_t)q_p.slot * kQKs;
+            q_p.next();
+            mma_run(tmem + L::cP + pb * C, a, b, idP, 8, hh > 0, [](int kk) { return kmajor_step(kk, C); },
+                    [](int kk) { return kmajor_step(kk, C); });
           }
-          mma_commit(bar(L::bPFull + pb));
+          mma_commit(bPFull + 8 * pb);
           return true;
         };
         // state update of half hh, then O (+)= Q_hh Sb_hh
         auto issue_s_qs = [&](int i, int hh) -> bool {
-          const int vs = i % NV, ob = i % NO, u = i * H + hh, b = u % NSB;
+          const int ob = i & (NO - 1), u = i * H + hh, b = u & (NSB - 1);
           if (hh == 0) {
-            if (!wait(L::bWReady + vs, i / NV)) return false;
-            if (!fast && !wait(L::bVFull + vs, i / NV)) return false;
+            if (!wait(bWReady + 8 * v_s.slot, v_s.phase)) return false;
+            if (!fast && !wait(bVFull + 8 * v_s.slot, v_s.phase)) return false;
             if (fast) frame_advance(c, n, inv_g(i));
           }
-          if (!wait_qk(u + 1) || !wait(L::bSRead + hh, i)) return false;
+          if (!wait_qk(u + 1) || !wait(bSRead + 8 * hh, (uint32_t)i)) return false;
           tc_fence_after();
-          mma_s(i, hh, fast ? n : 0);
-          mma_commit(bar(L::bSFull + hh));
-          if (hh == 0 && i >= NO && !wait(L::bOFree + ob, i / NO - 1)) return false;
-          if (!wait(L::bSbReady + b, u / NSB)) return false;
+          mma_s(tmem + L::cS + hh * DVT, q_s.slot, v_s.slot, has_state(i), fast ? n : 0);
+          mma_commit(bSFull + 8 * hh);
+          if (hh == 0 && i >= NO && !wait(bOFree + 8 * ob, (uint32_t)(i / NO - 1))) return false;
+          if (!wait(bSbReady + 8 * b, (uint32_t)(u / NSB))) return false;
           tc_fence_after();
-          if (has_state(i)) {
-            const int s = u % NQK;
-            mma_run(tmem + L::cO + ob * DVT, make_sdesc(qk_q(s), 16, 1024), make_sdesc(sb_buf(b), 128 * 128, 1024),
-                    idO, 8, hh > 0, [](int kk) { return kmajor_step(kk, C); }, [](int kk) { return (uint32_t)kk * 2048; });
-          }
-          if (!L::kMergeSbFree) mma_commit(bar(L::bSbFree + b));
-          mma_commit(bar(L::bQkEmpty + u % NQK));  // the chunk's Q/K half is no longer read
+          if (has_state(i))
+            mma_run(tmem + L::cO + ob * DVT, dQ + (uint64_t)q_s.slot * kQKs, dSb + (uint64_t)b * kSbs, idO, 8,
+                    hh > 0, [](int kk) { return kmajor_step(kk, C); }, [](int kk) { return (uint32_t)kk * 2048; });
+          if (!L::kMergeSbFree) mma_commit(bSbFree + 8 * b);
+          mma_commit(bQkEmpty + 8 * q_s.slot);  // the chunk's Q/K half is no longer read
+          q_s.next();
+          if (hh == H - 1) v_s.next();
           return true;
         };
         // O += P~ W, P~ read from tensor memory
         auto issue_pw = [&](int i) -> bool {
-          const int ob = i % NO, pb = i % NP, vs = i % NV;
-          if (!wait(L::bPtReady + pb, i / NP)) return false;
+          const int ob = i & (NO - 1), pb = i & (NP - 1);
+          if (!wait(bPtReady + 8 * pb, (uint32_t)(i / NP))) return false;
           tc_fence_after();
-          {
-            const uint64_t db = make_sdesc(v_slot(vs), C * 128, 1024);
-            const uint32_t dO = tmem + L::cO + ob * DVT, aP = tmem + L::cP + pb * C;
-            mma_bf16_ta(dO, aP, db, idO, has_state(i) ? 1u : 0u);
+          const uint64_t db = dV + (uint64_t)v_w.slot * kVs;
+          const uint32_t dO = tmem + L::cO + ob * DVT, aP = tmem + L::cP + pb * C;
+          mma_bf16_ta(dO, aP, db, idO, has_state(i) ? 1u : 0u);
 #pragma unroll
-            for (int kk = 1; kk < C / 16; ++kk) mma_bf16_ta(dO, aP + kk * 8, desc_add(db, kk * 2048), idO, 1u);
-          }
-          mma_commit(bar(L::bOFull + ob));
-          if (!L::kMergePFree) mma_commit(bar(L::bPFree + pb));
-          if (L::kSepStage) mma_commit(bar(L::bVEmpty + vs));  // V slot free once the MMAs are done
+          for (int kk = 1; kk < C / 16; ++kk) mma_bf16_ta(dO, aP + kk * 8, db + kk * 128, idO, 1u);
+          mma_commit(bOFull + 8 * ob);
+          if (!L::kMergePFree) mma_commit(bPFree + 8 * pb);
+          if (L::kSepStage) mma_commit(bVEmpty + 8 * v_w.slot);  // V slot free once the MMAs are done
+          v_w.next();
           return true;
         };
         auto issue_s_all = [&](int i) -> bool {
