@@ -653,16 +653,31 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           float acc[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-          for (int t = 0; t < seg; ++t) {
-            const float f = gamma_pow(g, lg, (float)(seg - 1 - t) * seg_len);
-            const float4* src = ws_block(t, hh) + (size_t)(cb * 8) * 128 + srow;
+          // three segments' loads in flight per round trip (the blocks are
+          // L2 hits, so latency, not bandwidth, sets the cost)
+#pragma unroll 1
+          for (int t0 = 0; t0 < seg; t0 += 3) {
+            float4 x[3][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 x = src[j * 128];
-              acc[4 * j + 0] = fmaf(f, x.x, acc[4 * j + 0]);
-              acc[4 * j + 1] = fmaf(f, x.y, acc[4 * j + 1]);
-              acc[4 * j + 2] = fmaf(f, x.z, acc[4 * j + 2]);
-              acc[4 * j + 3] = fmaf(f, x.w, acc[4 * j + 3]);
+            for (int tt = 0; tt < 3; ++tt) {
+              if (t0 + tt < seg) {
+                const float4* src = ws_block(t0 + tt, hh) + (size_t)(cb * 8) * 128 + srow;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[tt][j] = __ldcg(src + j * 128);
+              }
+            }
+#pragma unroll
+            for (int tt = 0; tt < 3; ++tt) {
+              if (t0 + tt < seg) {
+                const float f = gamma_pow(g, lg, (float)(seg - 1 - t0 - tt) * seg_len);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  acc[4 * j + 0] = fmaf(f, x[tt][j].x, acc[4 * j + 0]);
+                  acc[4 * j + 1] = fmaf(f, x[tt][j].y, acc[4 * j + 1]);
+                  acc[4 * j + 2] = fmaf(f, x[tt][j].z, acc[4 * j + 2]);
+                  acc[4 * j + 3] = fmaf(f, x[tt][j].w, acc[4 * j + 3]);
+                }
+              }
             }
           }
           uint32_t r[32];
@@ -885,9 +900,12 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           tc_fence_before();
           mbar_arrive(bar(L::bOFree + ob));  // the next product may overwrite O now
         }
-        // the staging buffer is free once the previous store has read it (the
-        // thread that issued that store waited for this before the barrier)
-        if (L::kSepStage && cb == 0) named_bar_sync(kBarO, kGroup);
+        // the staging buffer is free once the previous store has read it: the
+        // thread that issued that store waits for this before the barrier
+        if (L::kSepStage && cb == 0) {
+          if (eo == 0) bulk_wait_group_read0();
+          named_bar_sync(kBarO, kGroup);
+        }
         if (arow >= 0) {
           uint32_t pk[32];
 #pragma unroll
@@ -905,8 +923,10 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         for (int b = 0; b < DVT / 64; ++b)
           tma_store_3d(x.tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, row0, bh);
         bulk_commit_group();
-        bulk_wait_group_read0();  // the buffer may be rewritten once the store has read it
-        if (!L::kSepStage) mbar_arrive(bar(L::bVEmpty + vs));
+        if (!L::kSepStage) {
+          bulk_wait_group_read0();  // the V slot may be reloaded once the store has read it
+          mbar_arrive(bar(L::bVEmpty + vs));
+        }
       }
       return true;
     };
