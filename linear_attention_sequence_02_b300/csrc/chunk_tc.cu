@@ -31,10 +31,12 @@
 // K <- diag(gamma^(L-1-m)) K and Q <- diag(scale gamma^(t+1)) Q, so that
 //   S_i = gamma^L S_{i-1} + K^T V,   out = P~ V + Q S_{i-1}.
 //
-// Roles in a CTA of 320 threads:
+// Roles in a CTA of 352 threads:
 //   warp 0 lane 0 : TMA producer: V tiles and 128-column halves of Q and K into
 //                   two shared-memory rings
-//   warp 1        : owns the TMEM allocation; lane 0 issues every tcgen05.mma
+//   warp 1        : owns the TMEM allocation; lane 0 issues Q K^T and the
+//                   state update (every MMA of the state-only pre-pass)
+//   warp 10 lane 0: issues Q S and P~ W, the products accumulated into O
 //   warps 2..5    : state group: W = diag(w) V in place, the bf16 snapshot of
 //                   the state for the Q S product, the initial and final states
 //   warps 6..9    : output group: causal mask of P = Q K^T into bf16 in place in
@@ -75,7 +77,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kIssuerWarpB = 10;                  // warp of the second MMA issuer
 constexpr int kGroup = 128;                         // threads of one epilogue group
 constexpr uint32_t kBarS = 1, kBarO = 2;            // named barrier ids of the two groups
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
@@ -165,7 +168,7 @@ struct Cfg {
                        bWReady = 2 * NQK + 2 * NV, bSRead = 2 * NQK + 3 * NV, bSFull = bSRead + H,
                        bSbReady = bSFull + H, bSbFree = bSbReady + NSB, bPFull = bSbFree + NSB,
                        bPFree = bPFull + NP, bPtReady = bPFree + NP, bOFull = bPtReady + NP,
-                       bOFree = bOFull + NO, bFin = bOFree + NO, kBars = bFin + 1;
+                       bOFree = bOFull + NO, bFin = bOFree + NO, bSDone = bFin + 1, kBars = bSDone + NV;
   static_assert(kBars * 8 <= kBarBytes, "barriers");
 };
 
@@ -480,13 +483,19 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       for (int u = qk_issued - 1; u >= 0 && u >= qk_issued - NQK; --u)
         drain_bar(bar(L::bQkFull + u % NQK), (u / NQK) & 1, abort_flag);
     }
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
-    // One thread issues every MMA.  Its loop is a chain of dependent
-    // instructions with nothing on its SMSP to hide their latency, so ring
-    // slots and parities are running counters (no division) and operand
-    // descriptors are a per-ring base plus slot stride.
-    if (lane == 0) {
+  } else if (warp == 1 || warp == kIssuerWarpB) {
+    // ================= MMA issuers =================
+    // Two threads issue the MMAs, each a chain of dependent instructions
+    // (waits, bookkeeping, MMAs): lane 0 of warp 1 (A) issues Q K^T and the
+    // state update, lane 0 of warp kIssuerWarpB (B) the two products that
+    // accumulate into O, Q S and P~ W, so the O accumulator keeps one issue
+    // order.  The state-only pass has A alone.  Slots both read are freed
+    // by a commit from each; B issues P~ W(i) only after the state update of
+    // chunk i (which also reads W) has completed, so its release of the V
+    // slot (or the output group's, when outputs are staged in the slot)
+    // covers A's read too.  Ring slots and parities are running counters and
+    // operand descriptors a per-ring base plus slot stride.
+    if (lane == 0 && (warp == 1 || !SO)) {
       constexpr uint32_t idP = make_idesc(C, C, false, false);
       constexpr uint32_t idO = make_idesc(C, DVT, false, true);
       constexpr uint32_t idS = make_idesc(128, DVT, true, true);
@@ -500,138 +509,143 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
                      bVEmpty = bar(L::bVEmpty), bWReady = bar(L::bWReady), bSRead = bar(L::bSRead),
                      bSFull = bar(L::bSFull), bSbReady = bar(L::bSbReady), bSbFree = bar(L::bSbFree),
                      bPFull = bar(L::bPFull), bPFree = bar(L::kMergePFree ? L::bOFull : L::bPFree),
-                     bPtReady = bar(L::bPtReady), bOFull = bar(L::bOFull), bOFree = bar(L::bOFree);
+                     bPtReady = bar(L::bPtReady), bOFull = bar(L::bOFull), bOFree = bar(L::bOFree),
+                     bSDone = bar(L::bSDone);
       auto wait = [&](uint32_t b, uint32_t par) { return wait_bar(b, par & 1u, abort_flag); };
-      // state update of one half: S_h = 2^-n S_h + K_h^T W (S_h = K_h^T W when the state is zero)
-      auto mma_s = [&](uint32_t d, int qslot, int vslot, bool has_state, int n) {
-        const uint64_t a = dKa + (uint64_t)qslot * kQKs, b = dV + (uint64_t)vslot * kVs;
-        if (has_state) mma_bf16_scaled(d, a, b, idS, n);
-        else mma_bf16(d, a, b, idS, 0u);
-#pragma unroll
-        for (int kk = 1; kk < C / 16; ++kk) mma_bf16(d, a + kk * 128, b + kk * 128, idS, 1u);
-      };
+      auto has_state = [&](int i) { return i > 0 || !zero_init; };
       bool ok = true;
-      float c = 1.f;
-      int n = 0;
-      RingPos<NQK> qk_w;  // next Q/K unit to wait for
-      int qk_waited = 0;
-      auto wait_qk = [&](int u_end) -> bool {
-        while (qk_waited < u_end) {
-          if (!wait(bQkFull + 8 * qk_w.slot, qk_w.phase)) return false;
-          qk_w.next();
-          ++qk_waited;
-        }
-        return true;
-      };
-      if (SO) {
-        // state only: S in chunk order, each once its W (or K^) and, in the
-        // direct form, the decayed state are ready
-        RingPos<NV> v;
-        RingPos<NQK> qs;
-        for (int i = 0; i < nck && ok; ++i) {
-          if (fast) frame_advance(c, n, inv_g(i));
-          if (!wait(bWReady + 8 * v.slot, v.phase) || (!fast && !wait(bVFull + 8 * v.slot, v.phase))) {
-            ok = false;
-            break;
+      if (warp == 1) {
+        // ---------- issuer A: Q K^T and the state update ----------
+        // state update of one half: S_h = 2^-n S_h + K_h^T W (S_h = K_h^T W when the state is zero)
+        auto mma_s = [&](uint32_t d, int qslot, int vslot, bool hs, int n) {
+          const uint64_t a = dKa + (uint64_t)qslot * kQKs, b = dV + (uint64_t)vslot * kVs;
+          if (hs) mma_bf16_scaled(d, a, b, idS, n);
+          else mma_bf16(d, a, b, idS, 0u);
+#pragma unroll
+          for (int kk = 1; kk < C / 16; ++kk) mma_bf16(d, a + kk * 128, b + kk * 128, idS, 1u);
+        };
+        float c = 1.f;
+        int n = 0;
+        RingPos<NQK> qk_w;  // next Q/K unit to wait for
+        int qk_waited = 0;
+        auto wait_qk = [&](int u_end) -> bool {
+          while (qk_waited < u_end) {
+            if (!wait(bQkFull + 8 * qk_w.slot, qk_w.phase)) return false;
+            qk_w.next();
+            ++qk_waited;
           }
-          for (int hh = 0; hh < H && ok; ++hh) {
-            ok = wait_qk(i * H + hh + 1) && (fast || wait(bSRead + 8 * hh, (uint32_t)i));
-            if (!ok) break;
-            tc_fence_after();
-            mma_s(tmem + L::cS + hh * DVT, qs.slot, v.slot, i > 0, n);
-            if (!fast) mma_commit(bSFull + 8 * hh);
-            if (!L::kUnifiedStage) mma_commit(bQkEmpty + 8 * qs.slot);
-            qs.next();
-          }
-          if (ok) mma_commit(bVEmpty + 8 * v.slot);
-          v.next();
-        }
-      } else {
-        // Static issue order, chosen so that each wait is normally met by
-        // work issued an iteration earlier.  With lookahead (chunk i+1's Q K^T
-        // may run while chunk i still holds its P buffer), chunk i issues
-        //   S(i), Q S(i), P~ W(i-1), Q K^T(i+1);
-        // without, Q K^T(i), S(i), Q S(i), P~ W(i).  S and Q S go half by
-        // half, since with one snapshot buffer the copy of half 1 waits for
-        // the Q S product of half 0.
-        RingPos<NQK> q_p, q_s;  // Q/K slot of the next unit for Q K^T, and for S / Q S
-        RingPos<NV> v_s, v_w;   // V slot of the next chunk for S, and for P~ W
-        auto has_state = [&](int i) { return i > 0 || !zero_init; };
-        // P[j % NP] = Q_j K_j^T
-        auto issue_p = [&](int j) -> bool {
-          const int pb = j & (NP - 1);
-          if (j >= NP && !wait(bPFree + 8 * pb, (uint32_t)(j / NP - 1))) return false;
-          if (!wait_qk((j + 1) * H)) return false;
-          tc_fence_after();
-#pragma unroll 1
-          for (int hh = 0; hh < H; ++hh) {
-            const uint64_t a = dQ + (uint64_t)q_p.slot * kQKs, b = dKb + (uint64_t)q_p.slot * kQKs;
-            q_p.next();
-            mma_run(tmem + L::cP + pb * C, a, b, idP, 8, hh > 0, [](int kk) { return kmajor_step(kk, C); },
-                    [](int kk) { return kmajor_step(kk, C); });
-          }
-          mma_commit(bPFull + 8 * pb);
           return true;
         };
-        // state update of half hh, then O (+)= Q_hh Sb_hh
-        auto issue_s_qs = [&](int i, int hh) -> bool {
-          const int ob = i & (NO - 1), u = i * H + hh, b = u & (NSB - 1);
-          if (hh == 0) {
+        if (SO) {
+          // state only: S in chunk order, each once its W (or K^) and, in the
+          // direct form, the decayed state are ready
+          RingPos<NV> v;
+          RingPos<NQK> qs;
+          for (int i = 0; i < nck && ok; ++i) {
+            if (fast) frame_advance(c, n, inv_g(i));
+            if (!wait(bWReady + 8 * v.slot, v.phase) || (!fast && !wait(bVFull + 8 * v.slot, v.phase))) {
+              ok = false;
+              break;
+            }
+            for (int hh = 0; hh < H && ok; ++hh) {
+              ok = wait_qk(i * H + hh + 1) && (fast || wait(bSRead + 8 * hh, (uint32_t)i));
+              if (!ok) break;
+              tc_fence_after();
+              mma_s(tmem + L::cS + hh * DVT, qs.slot, v.slot, i > 0, n);
+              if (!fast) mma_commit(bSFull + 8 * hh);
+              if (!L::kUnifiedStage) mma_commit(bQkEmpty + 8 * qs.slot);
+              qs.next();
+            }
+            if (ok) mma_commit(bVEmpty + 8 * v.slot);
+            v.next();
+          }
+        } else {
+          // With lookahead (chunk i+1's Q K^T may run while chunk i still
+          // holds its P buffer) chunk i issues S(i), Q K^T(i+1); without,
+          // Q K^T(i), S(i).
+          RingPos<NQK> q_p, q_s;  // Q/K slot of the next unit for Q K^T, and for S
+          RingPos<NV> v_s;        // V slot of the next chunk for S
+          // P[j % NP] = Q_j K_j^T
+          auto issue_p = [&](int j) -> bool {
+            const int pb = j & (NP - 1);
+            if (j >= NP && !wait(bPFree + 8 * pb, (uint32_t)(j / NP - 1))) return false;
+            if (!wait_qk((j + 1) * H)) return false;
+            tc_fence_after();
+#pragma unroll 1
+            for (int hh = 0; hh < H; ++hh) {
+              const uint64_t a = dQ + (uint64_t)q_p.slot * kQKs, b = dKb + (uint64_t)q_p.slot * kQKs;
+              q_p.next();
+              mma_run(tmem + L::cP + pb * C, a, b, idP, 8, hh > 0, [](int kk) { return kmajor_step(kk, C); },
+                      [](int kk) { return kmajor_step(kk, C); });
+            }
+            mma_commit(bPFull + 8 * pb);
+            return true;
+          };
+          // state update of chunk i, half by half
+          auto issue_s = [&](int i) -> bool {
             if (!wait(bWReady + 8 * v_s.slot, v_s.phase)) return false;
             if (!fast && !wait(bVFull + 8 * v_s.slot, v_s.phase)) return false;
             if (fast) frame_advance(c, n, inv_g(i));
+            for (int hh = 0; hh < H; ++hh) {
+              if (!wait_qk(i * H + hh + 1) || !wait(bSRead + 8 * hh, (uint32_t)i)) return false;
+              tc_fence_after();
+              mma_s(tmem + L::cS + hh * DVT, q_s.slot, v_s.slot, has_state(i), fast ? n : 0);
+              mma_commit(bSFull + 8 * hh);
+              mma_commit(bQkEmpty + 8 * q_s.slot);  // A's reads of the Q/K half are done
+              q_s.next();
+            }
+            mma_commit(bSDone + 8 * v_s.slot);  // W of this V slot is no longer read by A
+            v_s.next();
+            return true;
+          };
+          // one call site per step keeps the issuer's code small
+          if (look) {
+            for (int i = -1; i < nck && ok; ++i) {
+              if (i >= 0) ok = issue_s(i);
+              if (ok && i + 1 < nck) ok = issue_p(i + 1);
+            }
+          } else {
+            for (int i = 0; i < nck && ok; ++i) ok = issue_p(i) && issue_s(i);
           }
-          if (!wait_qk(u + 1) || !wait(bSRead + 8 * hh, (uint32_t)i)) return false;
-          tc_fence_after();
-          mma_s(tmem + L::cS + hh * DVT, q_s.slot, v_s.slot, has_state(i), fast ? n : 0);
-          mma_commit(bSFull + 8 * hh);
-          if (hh == 0 && i >= NO && !wait(bOFree + 8 * ob, (uint32_t)(i / NO - 1))) return false;
-          if (!wait(bSbReady + 8 * b, (uint32_t)(u / NSB))) return false;
-          tc_fence_after();
-          if (has_state(i))
-            mma_run(tmem + L::cO + ob * DVT, dQ + (uint64_t)q_s.slot * kQKs, dSb + (uint64_t)b * kSbs, idO, 8,
-                    hh > 0, [](int kk) { return kmajor_step(kk, C); }, [](int kk) { return (uint32_t)kk * 2048; });
-          if (!L::kMergeSbFree) mma_commit(bSbFree + 8 * b);
-          mma_commit(bQkEmpty + 8 * q_s.slot);  // the chunk's Q/K half is no longer read
-          q_s.next();
-          if (hh == H - 1) v_s.next();
-          return true;
-        };
-        // O += P~ W, P~ read from tensor memory
-        auto issue_pw = [&](int i) -> bool {
+        }
+      } else {
+        // ---------- issuer B: O (+)= Q S, then O += P~ W ----------
+        RingPos<NQK> q_b;  // Q/K slot of the next unit for Q S
+        RingPos<NV> v_b;   // V slot of the next chunk
+        for (int i = 0; i < nck && ok; ++i) {
           const int ob = i & (NO - 1), pb = i & (NP - 1);
-          if (!wait(bPtReady + 8 * pb, (uint32_t)(i / NP))) return false;
+          // W (and, in the direct form, the scaled Q) of chunk i, and a free O buffer
+          ok = wait(bWReady + 8 * v_b.slot, v_b.phase) && (i < NO || wait(bOFree + 8 * ob, (uint32_t)(i / NO - 1)));
+          for (int hh = 0; hh < H && ok; ++hh) {
+            const int u = i * H + hh, b = u & (NSB - 1);
+            ok = wait(bQkFull + 8 * q_b.slot, q_b.phase) && wait(bSbReady + 8 * b, (uint32_t)(u / NSB));
+            if (!ok) break;
+            tc_fence_after();
+            if (has_state(i))
+              mma_run(tmem + L::cO + ob * DVT, dQ + (uint64_t)q_b.slot * kQKs, dSb + (uint64_t)b * kSbs, idO, 8,
+                      hh > 0, [](int kk) { return kmajor_step(kk, C); }, [](int kk) { return (uint32_t)kk * 2048; });
+            if (!L::kMergeSbFree) mma_commit(bSbFree + 8 * b);
+            mma_commit(bQkEmpty + 8 * q_b.slot);  // B's read of the Q half is done
+            q_b.next();
+          }
+          // P~ of chunk i, and its state update done with W
+          ok = ok && wait(bPtReady + 8 * pb, (uint32_t)(i / NP)) && wait(bSDone + 8 * v_b.slot, v_b.phase);
+          if (!ok) break;
           tc_fence_after();
-          const uint64_t db = dV + (uint64_t)v_w.slot * kVs;
+          const uint64_t db = dV + (uint64_t)v_b.slot * kVs;
           const uint32_t dO = tmem + L::cO + ob * DVT, aP = tmem + L::cP + pb * C;
           mma_bf16_ta(dO, aP, db, idO, has_state(i) ? 1u : 0u);
 #pragma unroll
           for (int kk = 1; kk < C / 16; ++kk) mma_bf16_ta(dO, aP + kk * 8, db + kk * 128, idO, 1u);
           mma_commit(bOFull + 8 * ob);
           if (!L::kMergePFree) mma_commit(bPFree + 8 * pb);
-          if (L::kSepStage) mma_commit(bVEmpty + 8 * v_w.slot);  // V slot free once the MMAs are done
-          v_w.next();
-          return true;
-        };
-        auto issue_s_all = [&](int i) -> bool {
-          for (int hh = 0; hh < H; ++hh)
-            if (!issue_s_qs(i, hh)) return false;
-          return true;
-        };
-        // one call site per step keeps the issuer's code small
-        if (look) {
-          for (int i = -1; i <= nck && ok; ++i) {
-            if (i >= 0 && i < nck) ok = issue_s_all(i);
-            if (ok && i >= 1) ok = issue_pw(i - 1);
-            if (ok && i + 1 < nck) ok = issue_p(i + 1);
-          }
-        } else {
-          for (int i = 0; i < nck && ok; ++i) ok = issue_p(i) && issue_s_all(i) && issue_pw(i);
+          if (L::kSepStage) mma_commit(bVEmpty + 8 * v_b.slot);  // V slot free once the MMAs are done
+          v_b.next();
         }
       }
-      // every issued MMA has completed before TMEM is released
+      // every MMA either thread issued has completed before TMEM is released
       mma_commit(bar(L::bFin));
-      drain_bar(bar(L::bFin), 0, abort_flag);
+      if (warp == 1) drain_bar(bar(L::bFin), 0, abort_flag);
     }
   } else if (warp < 6) {
     // ================= state group (warps 2..5) =================
@@ -980,7 +994,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int i = 0; i < NQK; ++i) {
       mbar_init(bar(L::bQkFull + i), 1);
-      mbar_init(bar(L::bQkEmpty + i), 1);
+      mbar_init(bar(L::bQkEmpty + i), SO ? 1 : 2);  // main pass: both issuers read the slot
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(bar(L::bVFull + i), 1);
@@ -1004,7 +1018,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
       mbar_init(bar(L::bOFull + i), 1);
       mbar_init(bar(L::bOFree + i), kGroup);
     }
-    mbar_init(bar(L::bFin), 1);
+    mbar_init(bar(L::bFin), SO ? 1 : 2);
+    for (int i = 0; i < NV; ++i) mbar_init(bar(L::bSDone + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
     if (!SO) prefetch_tensormap(&tmq);
