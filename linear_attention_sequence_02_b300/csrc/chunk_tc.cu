@@ -80,7 +80,8 @@ using namespace ptx;
 constexpr int kThreads = 352;
 constexpr int kIssuerWarpB = 10;                  // warp of the second MMA issuer
 constexpr int kGroup = 128;                         // threads of one epilogue group
-constexpr uint32_t kBarS = 1, kBarO = 2;            // named barrier ids of the two groups
+constexpr uint32_t kBarO = 2;                       // named barrier of the output group
+constexpr uint32_t kBarInit = 3;                    // state and output groups after the initial state
 constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s per wait
 constexpr float kMinChunkDecayLog2 = -14.0f;        // rescaled form: gamma^C >= 2^-14
 
@@ -439,6 +440,59 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     return len == C ? inv_gC : 1.f / pw[len];
   };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Initial state of a later segment: the decayed sum of the preceding
+  // segments' local end states (written by the pre-pass), state row `srow`,
+  // 32-column blocks cb0..cb1-1 of each half, into the state columns.  The
+  // state and output groups each take half the columns (the blocks are L2
+  // hits, so latency sets the cost: more threads, more loads in flight), then
+  // meet at a barrier of both groups.
+  auto init_state = [&](int srow, uint32_t lane_addr, int cb0, int cb1) {
+    griddep_wait();
+    const float seg_len = (float)p.seg_chunks * (float)C;
+#pragma unroll 1
+    for (int hh = 0; hh < H; ++hh) {
+#pragma unroll 1
+      for (int cb = cb0; cb < cb1; ++cb) {
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        // three segments' loads in flight per round trip
+#pragma unroll 1
+        for (int t0 = 0; t0 < seg; t0 += 3) {
+          float4 x[3][8];
+#pragma unroll
+          for (int tt = 0; tt < 3; ++tt) {
+            if (t0 + tt < seg) {
+              const float4* src = ws_block(t0 + tt, hh) + (size_t)(cb * 8) * 128 + srow;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) x[tt][j] = __ldcg(src + j * 128);
+            }
+          }
+#pragma unroll
+          for (int tt = 0; tt < 3; ++tt) {
+            if (t0 + tt < seg) {
+              const float f = gamma_pow(g, lg, (float)(seg - 1 - t0 - tt) * seg_len);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                acc[4 * j + 0] = fmaf(f, x[tt][j].x, acc[4 * j + 0]);
+                acc[4 * j + 1] = fmaf(f, x[tt][j].y, acc[4 * j + 1]);
+                acc[4 * j + 2] = fmaf(f, x[tt][j].z, acc[4 * j + 2]);
+                acc[4 * j + 3] = fmaf(f, x[tt][j].w, acc[4 * j + 3]);
+              }
+            }
+          }
+        }
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+        tmem_st32(tmem + lane_addr + L::cS + hh * DVT + cb * 32, r);
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();  // the other group reads these columns next
+    named_bar_sync(kBarInit, 2 * kGroup);
+    tc_fence_after();
+  };
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -653,55 +707,15 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     const int quarter = warp & 3;
     const uint32_t lane_addr = (uint32_t)(32 * quarter) << 16;
     const int srow = 32 * quarter + lane;  // state row inside a 128-row half
-    auto gw = [&](int b, uint32_t par) { return group_wait(kBarS, bar(b), par, abort_flag); };
+    // The group's waits are per warp (all lanes agree): the state group has no
+    // barrier of its own, so a warp that gives up strands no other, and no
+    // warp waits for the slowest of the four at every step.
+    auto gw = [&](int b, uint32_t par) {
+      const bool ok = wait_bar(bar(b), par & 1u, abort_flag);
+      return __all_sync(0xffffffffu, ok && !*abort_flag);
+    };
 
-    // initial state of a later segment: the decayed sum of the preceding
-    // segments' local end states (written by the pre-pass)
-    if (!zero_init) {
-      griddep_wait();
-      const float seg_len = (float)p.seg_chunks * (float)C;
-#pragma unroll 1
-      for (int hh = 0; hh < H; ++hh) {
-#pragma unroll 1
-        for (int cb = 0; cb < DVT / 32; ++cb) {
-          float acc[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-          // three segments' loads in flight per round trip (the blocks are
-          // L2 hits, so latency, not bandwidth, sets the cost)
-#pragma unroll 1
-          for (int t0 = 0; t0 < seg; t0 += 3) {
-            float4 x[3][8];
-#pragma unroll
-            for (int tt = 0; tt < 3; ++tt) {
-              if (t0 + tt < seg) {
-                const float4* src = ws_block(t0 + tt, hh) + (size_t)(cb * 8) * 128 + srow;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[tt][j] = __ldcg(src + j * 128);
-              }
-            }
-#pragma unroll
-            for (int tt = 0; tt < 3; ++tt) {
-              if (t0 + tt < seg) {
-                const float f = gamma_pow(g, lg, (float)(seg - 1 - t0 - tt) * seg_len);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  acc[4 * j + 0] = fmaf(f, x[tt][j].x, acc[4 * j + 0]);
-                  acc[4 * j + 1] = fmaf(f, x[tt][j].y, acc[4 * j + 1]);
-                  acc[4 * j + 2] = fmaf(f, x[tt][j].z, acc[4 * j + 2]);
-                  acc[4 * j + 3] = fmaf(f, x[tt][j].w, acc[4 * j + 3]);
-                }
-              }
-            }
-          }
-          uint32_t r[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
-          tmem_st32(tmem + lane_addr + L::cS + hh * DVT + cb * 32, r);
-        }
-      }
-      tmem_wait_st();
-    }
+    if (!zero_init) init_state(srow, lane_addr, 0, DVT / 64);
 
     // W = diag(c gamma^(L-1-m)) V, in place in the chunk's V slot
     auto w_pass = [&](int i, float ci) -> bool {
@@ -748,7 +762,28 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         uint8_t* sb = sm + L::oSb + b * L::kSb;
         if (u >= NSB && !gw(L::kMergeSbFree ? L::bOFull + b : L::bSbFree + b, (u / NSB - 1) & 1)) return false;
         if (has_state && i > 0 && !gw(L::bSFull + hh, (i - 1) & 1)) return false;
-        if (has_state) {
+        if (has_state && fast && DVT == 128) {
+          // the whole row in flight at once, so the state MMA is released
+          // before any of it is packed
+          tc_fence_after();
+          const float f = __uint_as_float((uint32_t)(127 - n) << 23);  // 2^-n
+          uint32_t r[128];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld32p(tS + q * 32, &r[q * 32]);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(L::bSRead + hh));  // the state MMA may overwrite S now
+#pragma unroll
+          for (int cb = 0; cb < 4; cb += 2) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              pk[j] = pack_bf16(f * __uint_as_float(r[cb * 32 + 2 * j]), f * __uint_as_float(r[cb * 32 + 2 * j + 1]));
+            store_row32_packed(sb, 128, srow, cb * 32, &pk[0]);
+            store_row32_packed(sb, 128, srow, cb * 32 + 32, &pk[16]);
+          }
+          fence_proxy_async_smem();
+        } else if (has_state) {
           tc_fence_after();
           const float f = fast ? __uint_as_float((uint32_t)(127 - n) << 23) : 1.f;  // 2^-n
 #pragma unroll 1
@@ -855,6 +890,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     const int quarter = warp & 3;
     const uint32_t lane_addr = (uint32_t)(32 * quarter) << 16;
     const int arow = acc_row(C, quarter, lane);  // token row of the C-row accumulators, -1 if none
+    if (!zero_init) init_state(32 * quarter + lane, lane_addr, DVT / 64, DVT / 32);
     auto go = [&](int b, uint32_t par) { return group_wait(kBarO, bar(b), par, abort_flag); };
 
     // P~ = causal mask of P (rescaled form) or (P (.) D) scale (direct form),
