@@ -85,6 +85,29 @@ int retention_chunkwise(const void *q, const void *k, const void *v, const float
                         int B, int H, int N, int dk, int dv, int chunk, void *stream);
 
 /*
+ * retention_chunkwise_from_state -- retention_chunkwise continued from a
+ * given state: the recurrence of "3. The Chunkwise Recurrent Representation
+ * ..." started from S_{-1} = state_in instead of zero, so that a sequence
+ * processed in pieces (chunked prefill) gives the same outputs and final
+ * state as one call on the whole sequence:
+ *
+ *   out_t  = scale [ sum_{m<=t} gamma^(t-m) (q_t . k_m) v_m + gamma^(t+1) q_t state_in ]
+ *   S_N-1  = gamma^N state_in + sum_m gamma^(N-1-m) k_m^T v_m         (scale = 1/sqrt(dk))
+ *
+ * state_in: float32 [B][H][dk][dv] row-major in device memory (the layout of
+ * state_out, e.g. the state_out of a call on the preceding tokens), 16-byte
+ * aligned, read only, owned by the caller; NULL means zero (then this is
+ * retention_chunkwise).  It must not overlap state_out (the call reads it
+ * while the last segment of the sequence writes state_out): state_in ==
+ * state_out returns RET_ERR_INVALID.  When N == 0, state_out receives a copy
+ * of state_in.  Everything else (shapes, workspace, errors) is as for
+ * retention_chunkwise.
+ */
+int retention_chunkwise_from_state(const void *q, const void *k, const void *v, const float *gamma,
+                                   const float *state_in, void *out, float *state_out,
+                                   int B, int H, int N, int dk, int dv, int chunk, void *stream);
+
+/*
  * retention_chunkwise_workspace_size -- bytes of scratch retention_chunkwise_ws
  * needs for this shape (0 when the plan does not split the sequence).
  * Host only; returns RET_ERR_INVALID / RET_ERR_UNSUPPORTED like

@@ -33,6 +33,7 @@ _fp = ctypes.POINTER(ctypes.c_float)
 # name -> argument types (all return int status unless noted)
 _SIGNATURES = {
     "retention_chunkwise": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+    "retention_chunkwise_from_state": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_chunkwise_ws": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                ctypes.c_size_t, _vp],
     "retention_chunkwise_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
@@ -148,6 +149,22 @@ def retention_chunkwise(q, k, v, gamma, chunk: int, out=None, state_out=None,
     args, out, state_out = _sequence_call("retention_chunkwise", torch.bfloat16, q, k, v, gamma,
                                           out, state_out, want_state, [int(chunk)], stream)
     _check("retention_chunkwise", lib().retention_chunkwise(*args, _stream(stream)))
+    return out, state_out
+
+
+def retention_chunkwise_from_state(q, k, v, gamma, chunk: int, state_in, out=None, state_out=None,
+                                   want_state: bool = True, stream=None):
+    """bf16 chunkwise forward continued from `state_in` (float32 [B, H, dk, dv]
+    CUDA tensor, or None for zero); returns (out, state_out or None)."""
+    args, out, state_out = _sequence_call("retention_chunkwise", torch.bfloat16, q, k, v, gamma,
+                                          out, state_out, want_state, [int(chunk)], stream)
+    if state_in is not None:
+        B, H, _, dk = q.shape
+        _need(state_in, "state_in", torch.float32, (B, H, dk, v.shape[-1]))
+    # (q, k, v, gamma, state_in, out, state_out, ...)
+    args = args[:4] + [_p(state_in)] + args[4:]
+    _check("retention_chunkwise_from_state",
+           lib().retention_chunkwise_from_state(*args, _stream(stream)))
     return out, state_out
 
 

@@ -63,6 +63,40 @@ int plan_chunkwise(int B, int H, int N, int dk, int dv, int chunk, int sms, ret:
   return RET_OK;
 }
 
+// bf16 chunkwise call that allocates its segment-state workspace
+// stream-ordered (cudaMallocAsync / cudaFreeAsync on the call's stream).
+int chunkwise_alloc(const void* q, const void* k, const void* v, const float* gamma,
+                    const float* state_in, void* out, float* state_out, int B, int H, int N, int dk,
+                    int dv, int chunk, void* stream) {
+  int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  ret::ChunkPlan plan;
+  const int sms = num_sms();
+  if (sms <= 0) return RET_ERR_CUDA;
+  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
+  if (st != RET_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    // the state after no tokens is the state before them
+    if (!state_out) return RET_OK;
+    if (!state_in) return zero_state(state_out, B, H, dk, dv, s);
+    return from_cuda(cudaMemcpyAsync(state_out, state_in, sizeof(float) * (size_t)B * H * dk * dv,
+                                     cudaMemcpyDeviceToDevice, s));
+  }
+  float* ws = nullptr;
+  if (plan.workspace_bytes > 0) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), plan.workspace_bytes, s) != cudaSuccess)
+      return RET_ERR_CUDA;
+  }
+  cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv,
+                                       chunk, plan, ws, s);
+  if (ws) {
+    cudaError_t e2 = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -132,34 +166,21 @@ int retention_chunkwise_ws(const void* q, const void* k, const void* v, const fl
     if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256))
       return RET_ERR_INVALID;
   }
-  return from_cuda(ret::launch_chunk_tc(q, k, v, gamma, out, state_out, B, H, N, dk, dv, chunk,
-                                        plan, static_cast<float*>(workspace), s));
+  return from_cuda(ret::launch_chunk_tc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv,
+                                        chunk, plan, static_cast<float*>(workspace), s));
 }
 
 int retention_chunkwise(const void* q, const void* k, const void* v, const float* gamma, void* out,
                         float* state_out, int B, int H, int N, int dk, int dv, int chunk,
                         void* stream) {
-  int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
-  if (st != RET_OK) return st;
-  ret::ChunkPlan plan;
-  const int sms = num_sms();
-  if (sms <= 0) return RET_ERR_CUDA;
-  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
-  if (st != RET_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (N == 0) return zero_state(state_out, B, H, dk, dv, s);
-  float* ws = nullptr;
-  if (plan.workspace_bytes > 0) {
-    if (cudaMallocAsync(reinterpret_cast<void**>(&ws), plan.workspace_bytes, s) != cudaSuccess)
-      return RET_ERR_CUDA;
-  }
-  cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, out, state_out, B, H, N, dk, dv, chunk,
-                                       plan, ws, s);
-  if (ws) {
-    cudaError_t e2 = cudaFreeAsync(ws, s);
-    if (e == cudaSuccess) e = e2;
-  }
-  return from_cuda(e);
+  return chunkwise_alloc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv, chunk, stream);
+}
+
+int retention_chunkwise_from_state(const void* q, const void* k, const void* v, const float* gamma,
+                                   const float* state_in, void* out, float* state_out, int B, int H,
+                                   int N, int dk, int dv, int chunk, void* stream) {
+  if (state_in && (!aligned(state_in, 16) || state_in == state_out)) return RET_ERR_INVALID;
+  return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, stream);
 }
 
 int retention_chunkwise_f32(const float* q, const float* k, const float* v, const float* gamma,

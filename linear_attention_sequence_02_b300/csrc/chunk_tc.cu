@@ -175,6 +175,7 @@ struct Cfg {
 
 struct TcParams {
   const float* gamma;
+  const float* state_in;  // state before the first token, [B*H][DK][dv] (null: zero)
   float* state_out;  // main pass: final state (may be null)
   float* ws;         // segment states [B*H][segments-1][DK][dv]
   int H, N, dv, n_dv_tiles, BH, segments, seg_chunks, n_chunks;
@@ -426,7 +427,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   const int dv0 = dvt * DVT;
   const float g = p.gamma[head];
   const float lg = g > 0.f ? log2f(g) : 0.f;
-  const bool zero_init = SO || seg == 0;
+  const bool zero_init = SO || (seg == 0 && p.state_in == nullptr);
   auto chunk_len = [&](int i) { return min(C, p.N - (c_begin + i) * C); };
   // Segment states in the workspace are stored lane-major: float4 number
   // (c4 * 128 + row) of block (bh, segment, dv tile, half) holds columns
@@ -440,14 +441,15 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     return len == C ? inv_gC : 1.f / pw[len];
   };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Initial state of a later segment: the decayed sum of the preceding
-  // segments' local end states (written by the pre-pass), state row `srow`,
-  // 32-column blocks cb0..cb1-1 of each half, into the state columns.  The
-  // state and output groups each take half the columns (the blocks are L2
-  // hits, so latency sets the cost: more threads, more loads in flight), then
-  // meet at a barrier of both groups.
+  // Initial state of a segment that does not start from zero: the caller's
+  // state, decayed to the segment's first token, plus the decayed sum of the
+  // preceding segments' local end states (written by the pre-pass); state
+  // row `srow`, 32-column blocks cb0..cb1-1 of each half, into the state
+  // columns.  The state and output groups each take half the columns (the
+  // blocks are L2 hits, so latency sets the cost: more threads, more loads in
+  // flight), then meet at a barrier of both groups.
   auto init_state = [&](int srow, uint32_t lane_addr, int cb0, int cb1) {
-    griddep_wait();
+    if (seg > 0) griddep_wait();  // the pre-pass wrote the workspace
     const float seg_len = (float)p.seg_chunks * (float)C;
 #pragma unroll 1
     for (int hh = 0; hh < H; ++hh) {
@@ -456,6 +458,20 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         float acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        if (p.state_in != nullptr) {
+          // gamma^(seg Lseg) state_in, row hh*128 + srow, columns dv0 + 32 cb ..
+          const float f = gamma_pow(g, lg, (float)seg * seg_len);
+          const float4* src = reinterpret_cast<const float4*>(
+              p.state_in + ((size_t)bh * DK + hh * 128 + srow) * p.dv + dv0 + cb * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = __ldg(src + j);
+            acc[4 * j + 0] = f * x.x;
+            acc[4 * j + 1] = f * x.y;
+            acc[4 * j + 2] = f * x.z;
+            acc[4 * j + 3] = f * x.w;
+          }
+        }
         // three segments' loads in flight per round trip
 #pragma unroll 1
         for (int t0 = 0; t0 < seg; t0 += 3) {
@@ -1207,8 +1223,9 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   return true;
 }
 
-cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma, void* out,
-                            float* state_out, int B, int H, int N, int dk, int dv, int chunk,
+cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
+                            const float* state_in, void* out, float* state_out, int B, int H, int N,
+                            int dk, int dv, int chunk,
                             const ChunkPlan& plan, float* workspace, cudaStream_t s) {
   const int BH = B * H;
   CUtensorMap mq, mk, mv, mo;
@@ -1217,6 +1234,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     return cudaErrorInvalidValue;
   TcParams p;
   p.gamma = gamma;
+  p.state_in = state_in;
   p.state_out = state_out;
   p.ws = workspace;
   p.H = H;

@@ -40,9 +40,11 @@ struct ChunkPlan {
 };
 // Fills `plan` for a supported shape; returns false for unsupported shapes.
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan);
+// state_in (nullable) is the state before the first token, [B*H][dk][dv].
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
-                            void* out, float* state_out, int B, int H, int N, int dk, int dv,
-                            int chunk, const ChunkPlan& plan, float* workspace, cudaStream_t s);
+                            const float* state_in, void* out, float* state_out, int B, int H,
+                            int N, int dk, int dv, int chunk, const ChunkPlan& plan,
+                            float* workspace, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 
 }  // namespace ret

@@ -84,3 +84,16 @@ def test_f32_and_parallel_and_step_validation(lib):
     assert lib.retention_step_f32(P, P, P, P, P_ODD, 1, 1, 32, 32, None) == binding.RET_ERR_INVALID
     assert lib.retention_gamma_schedule(0, None) == binding.RET_ERR_INVALID
     assert lib.retention_device_status(None, 0) == binding.RET_ERR_INVALID
+
+
+def test_chunkwise_from_state_validation(lib):
+    """Checked on the host before anything is enqueued: the starting state must
+    be 16-byte aligned and must not be the state_out buffer; the checks of
+    retention_chunkwise apply as well."""
+    P2 = ctypes.c_void_p(0x2000)
+    fs = lib.retention_chunkwise_from_state
+    # (q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, stream)
+    assert fs(P, P, P, P, P_ODD, P, P2, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
+    assert fs(P, P, P, P, P2, P, P2, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
+    assert fs(None, P, P, P, P2, P, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
+    assert fs(P, P, P, P, P2, P_ODD, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
