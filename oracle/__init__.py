@@ -13,6 +13,8 @@ Functions (see the C file for the formulas and the page sections they follow):
   parallel_rows(q, k, v, g, rows)  selected rows of the parallel form, one head
   recurrent(q, k, v, gamma, state=None)  recurrent form, returns (out, state)
   chunkwise(q, k, v, gamma, chunk, state_in=None)  returns (out, state)
+  groupnorm(r, weight=None, bias=None, eps=1e-6)  per-(token, head)
+                               normalisation, heads concatenated per token
 
 Every function here is pinned by tests/test_oracle.py against closed forms,
 hand-expanded sums, a library-routine special case and the three-form
@@ -85,6 +87,8 @@ class Oracle:
         lib.oracle_recurrent.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp] + [ctypes.c_int] * 5
         lib.oracle_chunkwise.restype = None
         lib.oracle_chunkwise.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp] + [ctypes.c_int] * 6
+        lib.oracle_groupnorm.restype = None
+        lib.oracle_groupnorm.argtypes = [_dp, _dp, _dp, _dp] + [ctypes.c_int] * 4 + [ctypes.c_double]
         self.lib = lib
 
     def threads(self) -> int:
@@ -142,6 +146,19 @@ class Oracle:
         return out, S
 
 
+    def groupnorm(self, r, weight=None, bias=None, eps: float = 1e-6) -> np.ndarray:
+        """Per-(token, head) normalisation of retention outputs r [B,H,N,dv]
+        with heads concatenated per token: returns y [B,N,H,dv] (fp64)."""
+        r = _f64(r)
+        B, H, N, dv = r.shape
+        w = None if weight is None else _f64(weight)
+        b = None if bias is None else _f64(bias)
+        y = np.zeros((B, N, H, dv), dtype=np.float64)
+        self.lib.oracle_groupnorm(_ptr(r), None if w is None else _ptr(w), None if b is None else _ptr(b),
+                                  _ptr(y), B, H, N, dv, float(eps))
+        return y
+
+
 def default() -> Oracle:
     """The oracle compiled from retention_oracle.c beside this file."""
     global _default
@@ -173,3 +190,7 @@ def recurrent(q, k, v, gammas, state=None):
 
 def chunkwise(q, k, v, gammas, chunk, state_in=None):
     return default().chunkwise(q, k, v, gammas, chunk, state_in)
+
+
+def groupnorm(r, weight=None, bias=None, eps=1e-6):
+    return default().groupnorm(r, weight, bias, eps)

@@ -244,3 +244,40 @@ void oracle_chunkwise(const double *q, const double *k, const double *v,
         }
     }
 }
+
+/*
+ * [G] "1. The Parallel Representation for High-Throughput Pretraining":
+ * MSR(X) = GroupNorm(Concat(R_1, ..., R_H)) W_O, and [G] "1. PyTorch
+ * Implementation of MultiScaleRetention": the normalisation has one group per
+ * head over the concatenated channels (num_groups = H, num_channels = H dv,
+ * eps = 1e-6 there; eps is an argument here), i.e. for every token n and head
+ * h, over the dv channels c of R_h:
+ *
+ *   mu = (1/dv) sum_c R[h][n][c]      var = (1/dv) sum_c (R[h][n][c] - mu)^2
+ *   Y[n][h][c] = (R[h][n][c] - mu) / sqrt(var + eps) * weight[h dv + c] + bias[h dv + c]
+ *
+ * r is [B][H][N][dv]; y is written with the heads concatenated per token,
+ * [B][N][H][dv].  weight and bias may be NULL (one and zero).
+ */
+void oracle_groupnorm(const double *r, const double *weight, const double *bias,
+                      double *y, int B, int H, int N, int dv, double eps)
+{
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h)
+      for (int n = 0; n < N; ++n) {
+        const double *x = r + (((size_t)b * H + h) * N + n) * dv;
+        double *out = y + (((size_t)b * N + n) * H + h) * dv;
+        double mu = 0.0;
+        for (int c = 0; c < dv; ++c) mu += x[c];
+        mu /= dv;
+        double var = 0.0;
+        for (int c = 0; c < dv; ++c) var += (x[c] - mu) * (x[c] - mu);
+        var /= dv;
+        const double inv = 1.0 / sqrt(var + eps);
+        for (int c = 0; c < dv; ++c) {
+          const double w = weight ? weight[h * dv + c] : 1.0;
+          const double bb = bias ? bias[h * dv + c] : 0.0;
+          out[c] = (x[c] - mu) * inv * w + bb;
+        }
+      }
+}

@@ -251,6 +251,46 @@ def check_empty_sequence(o):
     assert np.array_equal(S2, S0)
 
 
+# --- the normalisation of the heads' outputs -----------------------------------
+
+def check_groupnorm_is_the_library_group_norm(o):
+    """Per-(token, head) normalisation == torch.nn.functional.group_norm with
+    one group per head over the concatenated head channels (fp64, CPU), with a
+    random affine and two values of eps (the large one would expose eps
+    applied outside the square root)."""
+    import torch
+    B, H, N, dv = 2, 3, 7, 12
+    r = _rand((B, H, N, dv), 50) * 3.0 + 0.5
+    w, bias = _rand((H * dv,), 51), _rand((H * dv,), 52)
+    for eps in (1e-6, 0.5):
+        y = o.groupnorm(r, w, bias, eps)
+        x = torch.from_numpy(np.ascontiguousarray(r.transpose(0, 2, 1, 3))).reshape(B * N, H * dv)
+        ref = torch.nn.functional.group_norm(x, H, torch.from_numpy(w), torch.from_numpy(bias), eps)
+        _close(y, ref.reshape(B, N, H, dv).numpy(), 1e-13, f"groupnorm vs library, eps {eps}")
+
+
+def check_groupnorm_invariants(o):
+    """Constant groups give the bias; without an affine every group has mean 0
+    and mean square var/(var+eps); with eps = 0 the result ignores a positive
+    scale and a shift of each group; permuting heads permutes the output's head
+    axis."""
+    B, H, N, dv = 1, 2, 5, 8
+    bias = _rand((H * dv,), 60)
+    const = np.broadcast_to(_rand((B, H, N, 1), 61), (B, H, N, dv)).copy()
+    y = o.groupnorm(const, _rand((H * dv,), 62), bias, 1e-6)
+    # (x - mu is a rounding error of the mean, magnified by 1/sqrt(eps))
+    _close(y, np.broadcast_to(bias.reshape(1, 1, H, dv), y.shape), 1e-10, "groupnorm of constants")
+    r = _rand((B, H, N, dv), 63)
+    y = o.groupnorm(r, None, None, 1e-6)
+    var = r.var(axis=-1).transpose(0, 2, 1)
+    assert np.max(np.abs(y.mean(axis=-1))) < 1e-14
+    _close((y ** 2).mean(axis=-1), var / (var + 1e-6), 1e-13, "groupnorm mean square")
+    _close(o.groupnorm(7.5 * r - 2.0, None, None, 0.0), o.groupnorm(r, None, None, 0.0), 1e-12,
+           "groupnorm scale and shift")
+    yp = o.groupnorm(r[:, ::-1].copy(), None, None, 1e-6)
+    _close(yp, y[:, :, ::-1], 0.0, "groupnorm head permutation")
+
+
 ALL_CHECKS = [
     check_gamma_printed,
     check_hand_expanded_scalar,
@@ -264,4 +304,6 @@ ALL_CHECKS = [
     check_linearity_and_heads,
     check_state_continuation,
     check_empty_sequence,
+    check_groupnorm_is_the_library_group_norm,
+    check_groupnorm_invariants,
 ]

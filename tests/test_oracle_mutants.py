@@ -39,6 +39,9 @@ MUTANTS = {
     "chunk_inner_transposed": ("dot(qj, K + (size_t)(s + l) * dk, dk) * scale;",
                                "dot(Q + (size_t)(s + l) * dk, K + (size_t)(s + j) * dk, dk) * scale;"),
     "chunk_cross_term_dropped": ("oj[c] += zeta * scale * t;", "oj[c] += 0.0 * t;"),
+    "groupnorm_unbiased_variance": ("var /= dv;", "var /= (dv - 1);"),
+    "groupnorm_eps_outside_root": ("1.0 / sqrt(var + eps);", "1.0 / (sqrt(var) + eps);"),
+    "groupnorm_weight_of_head_0": ("weight[h * dv + c]", "weight[c]"),
 }
 
 
