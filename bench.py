@@ -346,6 +346,33 @@ def time_decode(w, reps, dev, seed=0):
     return times
 
 
+GROUPNORM = dict(name="groupnorm", B=4, H=8, N=2048, dv=128)  # the mid workload's output
+
+
+def time_groupnorm(w, reps, dev, flush, seed=0):
+    """ms per retention_groupnorm call on a [B,H,N,dv] bf16 input, L2 flushed first."""
+    from linear_attention_sequence_02_b300 import binding
+    B, H, N, dv = w["B"], w["H"], w["N"], w["dv"]
+    g = torch.Generator().manual_seed(seed)
+    r = torch.randn(B, H, N, dv, generator=g).to(torch.bfloat16).to(dev)
+    wt = torch.randn(H * dv, generator=g).to(dev)
+    bs = torch.randn(H * dv, generator=g).to(dev)
+    y = torch.empty(B, N, H, dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        binding.retention_groupnorm(r, wt, bs, 1e-6, out=y)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.retention_groupnorm(r, wt, bs, 1e-6, out=y)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    return times
+
+
 def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
     """fp64 oracle (chunkwise form, same chunk) on the full workload, repeated for >= min_seconds."""
     import oracle
@@ -420,6 +447,17 @@ def run_ours(args):
                          "traffic": recorded_traffic("decode_step")},
             "gpu_launches": DECODE["T"] * 3,
         }
+        gw = GROUPNORM
+        gt = statistics.median(time_groupnorm(gw, 20, dev, flush)) / 1e3
+        rows = gw["B"] * gw["H"] * gw["N"]
+        gbytes = 4 * gw["dv"] * rows  # bf16 row read + bf16 row written
+        extra["groupnorm"] = {
+            "rows_per_s": round(rows / gt, 1), "ms_per_call": round(gt * 1e3, 5),
+            "config": {k: gw[k] for k in ("B", "H", "N", "dv")} | {"l2": "flushed before each call",
+                                                                   "timing": "CUDA events per call"},
+            "roofline": {"bound": "hbm", "achieved": round(gbytes / gt / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbytes / gt / 1e9 / hbm, 4), "traffic": recorded_traffic("groupnorm")},
+            "gpu_launches": 1}
         for wl in (LONG, B7):
             t, n, _ = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
             a_s = statistics.median(t) / 1e3
@@ -501,8 +539,12 @@ def run_only(args):
         t = time_decode(DECODE, args.steps, dev)
         print(json.dumps({"only": "decode", "ms_per_step": statistics.median(t)}))
         return
-    w = {"mid": MID, "long": LONG, "7b": B7}[args.only]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.only == "groupnorm":
+        t = time_groupnorm(GROUPNORM, args.steps, dev, flush)
+        print(json.dumps({"only": "groupnorm", "ms_per_call": statistics.median(t), "launches": args.steps}))
+        return
+    w = {"mid": MID, "long": LONG, "7b": B7}[args.only]
     t, n, how = time_chunkwise(w, args.steps, args.warmup, dev, flush)
     print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": n, "timing": how}))
 
@@ -515,7 +557,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["mid", "long", "7b", "decode"], default=None)
+    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -108,6 +108,27 @@ int retention_chunkwise_from_state(const void *q, const void *k, const void *v, 
                                    int B, int H, int N, int dk, int dv, int chunk, void *stream);
 
 /*
+ * retention_groupnorm -- the normalisation of the heads' outputs that
+ * multi-scale retention applies before its output projection: "1. The
+ * Parallel Representation for High-Throughput Pretraining", MSR(X) =
+ * GroupNorm(Concat(R_1, ..., R_H)) W_O, with one group per head over the
+ * concatenated channels ("1. PyTorch Implementation of MultiScaleRetention").
+ * For every batch row b, token n and head h, over the dv channels c:
+ *
+ *   mu = mean_c r[b][h][n][c],   var = mean_c (r[b][h][n][c] - mu)^2
+ *   y[b][n][h][c] = (r[b][h][n][c] - mu) / sqrt(var + eps) * weight[h dv + c] + bias[h dv + c]
+ *
+ * r: bf16 [B][H][N][dv] (the retention output layout); y: bf16 [B][N][H][dv]
+ * (heads concatenated per token); both 16-byte aligned device memory and must
+ * not overlap.  weight, bias: float32 [H dv] device memory, or NULL for one and
+ * zero.  eps >= 0 (the pages use 1e-6).  Statistics in fp32.  dv must be a
+ * multiple of 4, at most 1024, and B H at most 65535 (else
+ * RET_ERR_UNSUPPORTED).  Asynchronous on `stream`; N == 0 is a no-op.
+ */
+int retention_groupnorm(const void *r, const float *weight, const float *bias, void *y,
+                        int B, int H, int N, int dv, float eps, void *stream);
+
+/*
  * retention_chunkwise_workspace_size -- bytes of scratch retention_chunkwise_ws
  * needs for this shape (0 when the plan does not split the sequence).
  * Host only; returns RET_ERR_INVALID / RET_ERR_UNSUPPORTED like

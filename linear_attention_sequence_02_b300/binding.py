@@ -42,6 +42,7 @@ _SIGNATURES = {
     "retention_chunkwise_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_parallel": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "retention_parallel_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "retention_groupnorm": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _vp],
     "retention_step": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_step_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_gamma_schedule": [_i, _fp],
@@ -235,6 +236,24 @@ def retention_parallel(q, k, v, gamma, out=None, stream=None):
 def retention_parallel_f32(q, k, v, gamma, out=None, stream=None):
     """fp32 parallel form; returns out."""
     return _parallel("retention_parallel_f32", torch.float32, q, k, v, gamma, out, stream)
+
+
+def retention_groupnorm(r, weight=None, bias=None, eps: float = 1e-6, out=None, stream=None):
+    """Per-(token, head) normalisation of bf16 retention outputs r [B, H, N, dv];
+    returns y [B, N, H, dv] (heads concatenated per token)."""
+    if r.dim() != 4:
+        raise ValueError("r must be [B, H, N, dv]")
+    B, H, N, dv = r.shape
+    _need(r, "r", torch.bfloat16, (B, H, N, dv))
+    for t, name in ((weight, "weight"), (bias, "bias")):
+        if t is not None:
+            _need(t, name, torch.float32, (H * dv,))
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=r.device)
+    _need(out, "out", torch.bfloat16, (B, N, H, dv))
+    _check("retention_groupnorm", lib().retention_groupnorm(_p(r), _p(weight), _p(bias), _p(out), B, H, N,
+                                                            dv, float(eps), _stream(stream)))
+    return out
 
 
 def _step(fn, dtype, q, k, v, state, out, stream):

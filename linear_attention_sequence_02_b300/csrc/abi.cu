@@ -197,6 +197,21 @@ int retention_chunkwise_f32(const float* q, const float* k, const float* v, cons
                                              chunk, s));
 }
 
+int retention_groupnorm(const void* r, const float* weight, const float* bias, void* y, int B, int H,
+                        int N, int dv, float eps, void* stream) {
+  if (B <= 0 || H <= 0 || N < 0 || dv <= 0) return RET_ERR_INVALID;
+  if (!(eps >= 0.f) || eps > 1e30f) return RET_ERR_INVALID;  // also rejects NaN
+  if ((int64_t)B * H > INT32_MAX) return RET_ERR_INVALID;
+  if (N > 0) {
+    if (!r || !y || !aligned(r, 16) || !aligned(y, 16)) return RET_ERR_INVALID;
+  }
+  if ((weight && !aligned(weight, 4)) || (bias && !aligned(bias, 4))) return RET_ERR_INVALID;
+  if (!ret::groupnorm_supported(dv) || (int64_t)B * H > 65535) return RET_ERR_UNSUPPORTED;
+  if (N == 0) return RET_OK;
+  return from_cuda(ret::launch_groupnorm_bf16(r, weight, bias, y, B, H, N, dv, eps,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int retention_parallel(const void* q, const void* k, const void* v, const float* gamma, void* out,
                        int B, int H, int N, int dk, int dv, void* stream) {
   int st = check_sequence(q, k, v, gamma, out, nullptr, B, H, N, dk, dv);

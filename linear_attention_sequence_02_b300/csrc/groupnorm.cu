@@ -1,0 +1,153 @@
+// groupnorm.cu -- the normalisation that follows multi-scale retention.
+//
+// "RetNet Guide: Retentive Networks & The Impossible Triangle", section "1. The
+// Parallel Representation for High-Throughput Pretraining": MSR(X) =
+// GroupNorm(Concat(R_1, ..., R_H)) W_O; section "1. PyTorch Implementation of
+// MultiScaleRetention": one group per head over the concatenated channels.
+// For every token n and head h, over the dv channels c of that head's output:
+//
+//   mu = mean_c R[h][n][c],  var = mean_c (R[h][n][c] - mu)^2
+//   Y[n][h][c] = (R[h][n][c] - mu) / sqrt(var + eps) * weight[h dv + c] + bias[h dv + c]
+//
+// R is the retention output layout [B][H][N][dv] (bf16); Y is written with the
+// heads concatenated per token, [B][N][H][dv] (bf16), the layout the output
+// projection reads.  A warp takes R consecutive rows of one (b, h) at a time:
+// coalesced reads of all R rows first (so R dv bf16 are in flight), then per row
+// two warp-shuffle reductions (mean, then the centred second moment) in fp32
+// and a coalesced write.  The kernel is bound by HBM: 4 dv bytes per row.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace ret {
+namespace {
+
+constexpr int kGnWarps = 8;  // rows in flight per CTA
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// G: 4-element groups per lane (dv <= 128 G); R: rows a warp has in flight at
+// once (their loads are issued together, so a warp keeps R dv bf16 in flight).
+// blockIdx.y is the (batch row, head) pair b H + h, so the head's affine is
+// loaded once per lane and no row index needs a division.
+template <int G, int R>
+__global__ void __launch_bounds__(kGnWarps * 32)
+groupnorm_kernel(const __nv_bfloat16* __restrict__ r, const float* __restrict__ weight,
+                 const float* __restrict__ bias, __nv_bfloat16* __restrict__ y, int H, int N, int dv,
+                 float eps) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int bh = blockIdx.y, h = bh % H, b = bh / H;
+  const int n4 = dv / 4;
+  const float inv_dv = 1.f / (float)dv;
+  // this lane's channels 4 (lane + 32 g) + e of head h, and their affine
+  float wv[G][4], bv[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int c4 = lane + 32 * g;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = h * dv + 4 * c4 + e;
+      const bool in = c4 < n4;
+      wv[g][e] = (in && weight) ? __ldg(weight + c) : 1.f;
+      bv[g][e] = (in && bias) ? __ldg(bias + c) : 0.f;
+    }
+  }
+  const __nv_bfloat16* rb = r + (size_t)bh * N * dv;                 // r[b][h][n][:] = rb + n dv
+  __nv_bfloat16* yb = y + ((size_t)b * N * H + h) * dv;              // y[b][n][h][:] = yb + n H dv
+  const size_t ys = (size_t)H * dv;
+  for (int n0 = (blockIdx.x * kGnWarps + warp) * R; n0 < N; n0 += gridDim.x * kGnWarps * R) {
+    float x[R][G][4];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const uint2* src = reinterpret_cast<const uint2*>(rb + (size_t)(n0 + j) * dv);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int c4 = lane + 32 * g;
+        if (n0 + j < N && c4 < n4) {
+          const uint2 u = __ldg(src + c4);
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+          x[j][g][0] = lo.x;
+          x[j][g][1] = lo.y;
+          x[j][g][2] = hi.x;
+          x[j][g][3] = hi.y;
+        } else {
+          x[j][g][0] = x[j][g][1] = x[j][g][2] = x[j][g][3] = 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (n0 + j >= N) break;
+      float s = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) s += (x[j][g][0] + x[j][g][1]) + (x[j][g][2] + x[j][g][3]);
+      const float mu = warp_sum(s) * inv_dv;
+      float q = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (lane + 32 * g < n4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float d = x[j][g][e] - mu;
+            q = fmaf(d, d, q);
+          }
+        }
+      }
+      const float inv = rsqrtf(warp_sum(q) * inv_dv + eps);
+      uint2* dst = reinterpret_cast<uint2*>(yb + (size_t)(n0 + j) * ys);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int c4 = lane + 32 * g;
+        if (c4 < n4) {
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[e] = fmaf((x[j][g][e] - mu) * inv, wv[g][e], bv[g][e]);
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
+          dst[c4] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+        }
+      }
+    }
+  }
+}
+
+template <int G, int R>
+cudaError_t launch_g(const void* r, const float* weight, const float* bias, void* y, int B, int H, int N,
+                     int dv, float eps, int sms, cudaStream_t s) {
+  // about eight CTAs per SM in all, at least one row block per CTA
+  const int per_bh = (N + kGnWarps * R - 1) / (kGnWarps * R);
+  const long long want_x = ((long long)sms * 8 + (long long)B * H - 1) / ((long long)B * H);
+  const int gx = (int)(want_x < per_bh ? (want_x < 1 ? 1 : want_x) : per_bh);
+  groupnorm_kernel<G, R><<<dim3(gx, B * H), kGnWarps * 32, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(r), weight, bias, static_cast<__nv_bfloat16*>(y), H, N, dv, eps);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool groupnorm_supported(int dv) { return dv > 0 && dv % 4 == 0 && dv <= 1024; }
+
+cudaError_t launch_groupnorm_bf16(const void* r, const float* weight, const float* bias, void* y, int B,
+                                  int H, int N, int dv, float eps, cudaStream_t s) {
+  if ((long long)B * H * N == 0) return cudaSuccess;
+  if ((long long)B * H > 65535) return cudaErrorInvalidConfiguration;  // grid.y
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dv <= 128) return launch_g<1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  if (dv <= 256) return launch_g<2, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  if (dv <= 512) return launch_g<4, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  return launch_g<8, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+}
+
+}  // namespace ret

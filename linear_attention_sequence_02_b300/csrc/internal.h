@@ -47,4 +47,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             float* workspace, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 
+// ---- normalisation of the heads' outputs (groupnorm.cu) -----------------------
+bool groupnorm_supported(int dv);
+cudaError_t launch_groupnorm_bf16(const void* r, const float* weight, const float* bias, void* y, int B,
+                                  int H, int N, int dv, float eps, cudaStream_t s);
+
 }  // namespace ret

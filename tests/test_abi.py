@@ -97,3 +97,16 @@ def test_chunkwise_from_state_validation(lib):
     assert fs(P, P, P, P, P2, P, P2, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
     assert fs(None, P, P, P, P2, P, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
     assert fs(P, P, P, P, P2, P_ODD, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
+
+
+def test_groupnorm_validation(lib):
+    gn = lib.retention_groupnorm
+    # (r, weight, bias, y, B, H, N, dv, eps, stream)
+    assert gn(None, None, None, P, 1, 1, 4, 128, 1e-6, None) == binding.RET_ERR_INVALID
+    assert gn(P_ODD, None, None, P, 1, 1, 4, 128, 1e-6, None) == binding.RET_ERR_INVALID
+    assert gn(P, None, None, P, 1, 1, 4, 128, -1.0, None) == binding.RET_ERR_INVALID
+    assert gn(P, None, None, P, 1, 1, 4, 128, float("nan"), None) == binding.RET_ERR_INVALID
+    assert gn(P, None, None, P, 0, 1, 4, 128, 1e-6, None) == binding.RET_ERR_INVALID
+    assert gn(P, ctypes.c_void_p(0x1002), None, P, 1, 1, 4, 128, 1e-6, None) == binding.RET_ERR_INVALID
+    assert gn(P, None, None, P, 1, 1, 4, 130, 1e-6, None) == binding.RET_ERR_UNSUPPORTED
+    assert gn(P, None, None, P, 1, 1, 4, 2048, 1e-6, None) == binding.RET_ERR_UNSUPPORTED
