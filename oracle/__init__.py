@@ -15,6 +15,7 @@ Functions (see the C file for the formulas and the page sections they follow):
   chunkwise(q, k, v, gamma, chunk, state_in=None)  returns (out, state)
   groupnorm(r, weight=None, bias=None, eps=1e-6)  per-(token, head)
                                normalisation, heads concatenated per token
+  rotate(x, theta, n0=0)       position phase rotation of queries or keys
 
 Every function here is pinned by tests/test_oracle.py against closed forms,
 hand-expanded sums, a library-routine special case and the three-form
@@ -87,6 +88,8 @@ class Oracle:
         lib.oracle_recurrent.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp] + [ctypes.c_int] * 5
         lib.oracle_chunkwise.restype = None
         lib.oracle_chunkwise.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp] + [ctypes.c_int] * 6
+        lib.oracle_rotate.restype = None
+        lib.oracle_rotate.argtypes = [_dp, _dp, _dp] + [ctypes.c_int] * 4 + [ctypes.c_long]
         lib.oracle_groupnorm.restype = None
         lib.oracle_groupnorm.argtypes = [_dp, _dp, _dp, _dp] + [ctypes.c_int] * 4 + [ctypes.c_double]
         self.lib = lib
@@ -159,6 +162,16 @@ class Oracle:
         return y
 
 
+    def rotate(self, x, theta, n0: int = 0) -> np.ndarray:
+        """Position phase rotation of x [B,H,N,d]: pair j of token n turned by
+        (n0 + n) theta_j; returns y [B,H,N,d] (fp64)."""
+        x, th = _f64(x), _f64(theta)
+        B, H, N, d = x.shape
+        y = np.zeros_like(x)
+        self.lib.oracle_rotate(_ptr(x), _ptr(th), _ptr(y), B, H, N, d, int(n0))
+        return y
+
+
 def default() -> Oracle:
     """The oracle compiled from retention_oracle.c beside this file."""
     global _default
@@ -194,3 +207,7 @@ def chunkwise(q, k, v, gammas, chunk, state_in=None):
 
 def groupnorm(r, weight=None, bias=None, eps=1e-6):
     return default().groupnorm(r, weight, bias, eps)
+
+
+def rotate(x, theta, n0=0):
+    return default().rotate(x, theta, n0)

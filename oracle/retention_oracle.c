@@ -281,3 +281,30 @@ void oracle_groupnorm(const double *r, const double *weight, const double *bias,
         }
       }
 }
+
+/*
+ * [G] "2. Relative Position via Complex Exponential Phase Rotations": the
+ * query and key at position n are multiplied by the phase e^(i n theta), so
+ * that their product depends on n - m only.  Reading R8 (design notes): pairs
+ * (2j, 2j+1) of the d real dimensions are the real and imaginary parts of one
+ * complex coordinate with frequency theta_j, and with the real dot product the
+ * kernels use, query and key are both rotated by the angle (n0 + n) theta_j,
+ * which makes q_n . k_m depend on n - m only.  x, y: [B][H][N][d] (d even),
+ * theta: [d/2]; n0 is the position of token 0.
+ */
+void oracle_rotate(const double *x, const double *theta, double *y, int B, int H, int N, int d,
+                   long n0)
+{
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h)
+      for (int n = 0; n < N; ++n) {
+        const double *xr = x + (((size_t)b * H + h) * N + n) * d;
+        double *yr = y + (((size_t)b * H + h) * N + n) * d;
+        for (int j = 0; j < d / 2; ++j) {
+          const double a = (double)(n0 + n) * theta[j];
+          const double c = cos(a), s = sin(a);
+          yr[2 * j] = xr[2 * j] * c - xr[2 * j + 1] * s;
+          yr[2 * j + 1] = xr[2 * j] * s + xr[2 * j + 1] * c;
+        }
+      }
+}

@@ -291,6 +291,41 @@ def check_groupnorm_invariants(o):
     _close(yp, y[:, :, ::-1], 0.0, "groupnorm head permutation")
 
 
+# --- the position phase rotation -------------------------------------------------
+
+def check_rotation_relative_position(o):
+    """Rotated query and key give scores that depend on n - m only (a shift of
+    both positions leaves every score unchanged), and equal the unrotated pair
+    with the key turned by (m - n) theta."""
+    d, N = 8, 9
+    th = np.abs(_rand((d // 2,), 70))
+    q, k = _rand((1, 1, N, d), 71), _rand((1, 1, N, d), 72)
+    s0 = o.rotate(q, th, 0)[0, 0] @ o.rotate(k, th, 0)[0, 0].T
+    s5 = o.rotate(q, th, 5)[0, 0] @ o.rotate(k, th, 5)[0, 0].T
+    _close(s5, s0, 1e-12, "rotation: shift invariance")
+    n, m = 6, 2
+    k_rel = o.rotate(k[:, :, m:m + 1], th, m - n)  # key turned by (m - n) theta
+    want = q[0, 0, n] @ k_rel[0, 0, 0]
+    _close(s0[n, m], want, 1e-12, "rotation: relative angle")
+
+
+def check_rotation_special_cases(o):
+    """Position 0 and theta = 0 are the identity; lengths of pairs are kept;
+    a quarter turn maps (1, 0) to (0, 1); rotations compose."""
+    x = _rand((2, 3, 4, 6), 73)
+    th = np.abs(_rand((3,), 74))
+    y = o.rotate(x, th, 0)
+    assert np.array_equal(y[:, :, 0], x[:, :, 0])
+    assert np.array_equal(o.rotate(x, np.zeros(3), 7), x)
+    _close(np.hypot(y[..., 0::2], y[..., 1::2]), np.hypot(x[..., 0::2], x[..., 1::2]), 1e-14,
+           "rotation keeps pair lengths")
+    e = np.array([1.0, 0.0]).reshape(1, 1, 1, 2)
+    _close(o.rotate(e, np.array([np.pi / 2]), 1), np.array([0.0, 1.0]).reshape(1, 1, 1, 2), 1e-15,
+           "quarter turn")
+    x1 = x[:, :, :1]
+    _close(o.rotate(o.rotate(x1, th, 3), th, 4), o.rotate(x1, th, 7), 1e-13, "rotations compose")
+
+
 ALL_CHECKS = [
     check_gamma_printed,
     check_hand_expanded_scalar,
@@ -306,4 +341,6 @@ ALL_CHECKS = [
     check_empty_sequence,
     check_groupnorm_is_the_library_group_norm,
     check_groupnorm_invariants,
+    check_rotation_relative_position,
+    check_rotation_special_cases,
 ]

@@ -42,6 +42,12 @@ MUTANTS = {
     "groupnorm_unbiased_variance": ("var /= dv;", "var /= (dv - 1);"),
     "groupnorm_eps_outside_root": ("1.0 / sqrt(var + eps);", "1.0 / (sqrt(var) + eps);"),
     "groupnorm_weight_of_head_0": ("weight[h * dv + c]", "weight[c]"),
+    "rotate_sine_sign": ("yr[2 * j] = xr[2 * j] * c - xr[2 * j + 1] * s;",
+                         "yr[2 * j] = xr[2 * j] * c + xr[2 * j + 1] * s;"),
+    "rotate_start_ignored": ("const double a = (double)(n0 + n) * theta[j];",
+                             "const double a = (double)n * theta[j];"),
+    "rotate_pairs_split": ("yr[2 * j + 1] = xr[2 * j] * s + xr[2 * j + 1] * c;",
+                           "yr[2 * j + 1] = xr[(2 * j + 2) % d] * s + xr[2 * j + 1] * c;"),
 }
 
 
