@@ -373,6 +373,32 @@ def time_groupnorm(w, reps, dev, flush, seed=0):
     return times
 
 
+ROTATE = dict(name="rotate", B=4, H=8, N=2048, d=128)  # the mid workload's queries
+
+
+def time_rotate(w, reps, dev, flush, seed=0):
+    """ms per retention_rotate call on a [B,H,N,d] bf16 input, L2 flushed first."""
+    from linear_attention_sequence_02_b300 import binding
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).to(dev)
+    th = torch.tensor([10000.0 ** (-2.0 * j / d) for j in range(d // 2)], dtype=torch.float32, device=dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        binding.retention_rotate(x, th, 0, out=y)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.retention_rotate(x, th, 0, out=y)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    return times
+
+
 def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
     """fp64 oracle (chunkwise form, same chunk) on the full workload, repeated for >= min_seconds."""
     import oracle
@@ -458,6 +484,17 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(gbytes / gt / 1e9, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbytes / gt / 1e9 / hbm, 4), "traffic": recorded_traffic("groupnorm")},
             "gpu_launches": 1}
+        rw = ROTATE
+        rt = statistics.median(time_rotate(rw, 20, dev, flush)) / 1e3
+        rrows = rw["B"] * rw["H"] * rw["N"]
+        rbytes = 4 * rw["d"] * rrows  # bf16 row read + bf16 row written
+        extra["rotate"] = {
+            "rows_per_s": round(rrows / rt, 1), "ms_per_call": round(rt * 1e3, 5),
+            "config": {k: rw[k] for k in ("B", "H", "N", "d")} | {"l2": "flushed before each call",
+                                                                  "timing": "CUDA events per call"},
+            "roofline": {"bound": "hbm", "achieved": round(rbytes / rt / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(rbytes / rt / 1e9 / hbm, 4), "traffic": None},
+            "gpu_launches": 1}
         for wl in (LONG, B7):
             t, n, _ = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
             a_s = statistics.median(t) / 1e3
@@ -540,9 +577,10 @@ def run_only(args):
         print(json.dumps({"only": "decode", "ms_per_step": statistics.median(t)}))
         return
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    if args.only == "groupnorm":
-        t = time_groupnorm(GROUPNORM, args.steps, dev, flush)
-        print(json.dumps({"only": "groupnorm", "ms_per_call": statistics.median(t), "launches": args.steps}))
+    if args.only in ("groupnorm", "rotate"):
+        fn, wl = (time_groupnorm, GROUPNORM) if args.only == "groupnorm" else (time_rotate, ROTATE)
+        t = fn(wl, args.steps, dev, flush)
+        print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps}))
         return
     w = {"mid": MID, "long": LONG, "7b": B7}[args.only]
     t, n, how = time_chunkwise(w, args.steps, args.warmup, dev, flush)
@@ -557,7 +595,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm"], default=None)
+    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -108,6 +108,28 @@ int retention_chunkwise_from_state(const void *q, const void *k, const void *v, 
                                    int B, int H, int N, int dk, int dv, int chunk, void *stream);
 
 /*
+ * retention_rotate -- the position phase rotation of queries or keys: "2.
+ * Relative Position via Complex Exponential Phase Rotations" multiplies the
+ * query and key of token n by e^(i n theta), so that their product depends on
+ * n - m only.  Pairs (2j, 2j+1) of the d real dimensions are one complex
+ * coordinate with frequency theta_j; with the real dot product that the
+ * retention calls use, queries and keys are both turned by a = (n0 + n) theta_j:
+ *
+ *   y[2j] = x[2j] cos a - x[2j+1] sin a,   y[2j+1] = x[2j] sin a + x[2j+1] cos a
+ *
+ * so rotate q and k with the same theta and n0 before retention_chunkwise,
+ * retention_parallel or retention_step (n0 = the position of the sequence's
+ * first token, e.g. the number of tokens already in the state).  x, y: bf16
+ * [B][H][N][d], 16-byte aligned device memory; y may be x (in place), other
+ * overlaps are not allowed.  theta: float32 [d/2] device memory (learnable on
+ * the pages; any values).  d must be a multiple of 8, n0 >= 0 and
+ * n0 + N <= 2^24 (else RET_ERR_UNSUPPORTED).  Angles are reduced modulo 2 pi in
+ * fp32 before the sine and cosine.  Asynchronous on `stream`.
+ */
+int retention_rotate(const void *x, const float *theta, void *y,
+                     int B, int H, int N, int d, int n0, void *stream);
+
+/*
  * retention_groupnorm -- the normalisation of the heads' outputs that
  * multi-scale retention applies before its output projection: "1. The
  * Parallel Representation for High-Throughput Pretraining", MSR(X) =

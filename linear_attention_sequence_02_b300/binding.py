@@ -43,6 +43,7 @@ _SIGNATURES = {
     "retention_parallel": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "retention_parallel_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "retention_groupnorm": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _vp],
+    "retention_rotate": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "retention_step": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_step_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_gamma_schedule": [_i, _fp],
@@ -253,6 +254,22 @@ def retention_groupnorm(r, weight=None, bias=None, eps: float = 1e-6, out=None, 
     _need(out, "out", torch.bfloat16, (B, N, H, dv))
     _check("retention_groupnorm", lib().retention_groupnorm(_p(r), _p(weight), _p(bias), _p(out), B, H, N,
                                                             dv, float(eps), _stream(stream)))
+    return out
+
+
+def retention_rotate(x, theta, n0: int = 0, out=None, stream=None):
+    """Position phase rotation of bf16 queries or keys x [B, H, N, d] with
+    frequencies theta (float32 [d/2] CUDA tensor); out may be x (in place)."""
+    if x.dim() != 4:
+        raise ValueError("x must be [B, H, N, d]")
+    B, H, N, d = x.shape
+    _need(x, "x", torch.bfloat16, (B, H, N, d))
+    _need(theta, "theta", torch.float32, (d // 2,))
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, (B, H, N, d))
+    _check("retention_rotate", lib().retention_rotate(_p(x), _p(theta), _p(out), B, H, N, d, int(n0),
+                                                      _stream(stream)))
     return out
 
 

@@ -197,6 +197,19 @@ int retention_chunkwise_f32(const float* q, const float* k, const float* v, cons
                                              chunk, s));
 }
 
+int retention_rotate(const void* x, const float* theta, void* y, int B, int H, int N, int d, int n0,
+                     void* stream) {
+  if (B <= 0 || H <= 0 || N < 0 || d <= 0 || n0 < 0) return RET_ERR_INVALID;
+  if ((int64_t)B * H > INT32_MAX) return RET_ERR_INVALID;
+  if (N > 0) {
+    if (!x || !theta || !y || !aligned(x, 16) || !aligned(y, 16) || !aligned(theta, 4))
+      return RET_ERR_INVALID;
+  }
+  if (!ret::rotate_supported(N, d, n0)) return RET_ERR_UNSUPPORTED;
+  if (N == 0) return RET_OK;
+  return from_cuda(ret::launch_rotate_bf16(x, theta, y, B, H, N, d, n0, static_cast<cudaStream_t>(stream)));
+}
+
 int retention_groupnorm(const void* r, const float* weight, const float* bias, void* y, int B, int H,
                         int N, int dv, float eps, void* stream) {
   if (B <= 0 || H <= 0 || N < 0 || dv <= 0) return RET_ERR_INVALID;

@@ -47,6 +47,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             float* workspace, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 
+// ---- position phase rotation of queries and keys (rotate.cu) -------------------
+bool rotate_supported(int N, int d, int n0);
+cudaError_t launch_rotate_bf16(const void* x, const float* theta, void* y, int B, int H, int N, int d,
+                               int n0, cudaStream_t s);
+
 // ---- normalisation of the heads' outputs (groupnorm.cu) -----------------------
 bool groupnorm_supported(int dv);
 cudaError_t launch_groupnorm_bf16(const void* r, const float* weight, const float* bias, void* y, int B,

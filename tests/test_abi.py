@@ -110,3 +110,13 @@ def test_groupnorm_validation(lib):
     assert gn(P, ctypes.c_void_p(0x1002), None, P, 1, 1, 4, 128, 1e-6, None) == binding.RET_ERR_INVALID
     assert gn(P, None, None, P, 1, 1, 4, 130, 1e-6, None) == binding.RET_ERR_UNSUPPORTED
     assert gn(P, None, None, P, 1, 1, 4, 2048, 1e-6, None) == binding.RET_ERR_UNSUPPORTED
+
+
+def test_rotate_validation(lib):
+    rot = lib.retention_rotate
+    # (x, theta, y, B, H, N, d, n0, stream)
+    assert rot(None, P, P, 1, 1, 4, 128, 0, None) == binding.RET_ERR_INVALID
+    assert rot(P_ODD, P, P, 1, 1, 4, 128, 0, None) == binding.RET_ERR_INVALID
+    assert rot(P, P, P, 1, 1, 4, 128, -1, None) == binding.RET_ERR_INVALID
+    assert rot(P, P, P, 1, 1, 4, 124, 0, None) == binding.RET_ERR_UNSUPPORTED
+    assert rot(P, P, P, 1, 1, 4, 128, (1 << 24) - 3, None) == binding.RET_ERR_UNSUPPORTED
