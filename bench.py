@@ -222,8 +222,9 @@ def max_over_ranks(x: float, world: int, device) -> float:
 # ---------------------------------------------------------------------------
 # our arm
 
-def time_chunkwise(w, steps, warmup, dev, flush, seed=0):
-    """Per-call device times (ms) of retention_chunkwise, L2 flushed between calls.
+def time_chunkwise(w, steps, warmup, dev, flush, seed=0, norm=False):
+    """Per-call device times (ms) of retention_chunkwise (with norm: of
+    retention_chunkwise_groupnorm, the GroupNorm fused in), L2 flushed between calls.
 
     The call (state-only pre-pass, main pass launched with programmatic
     dependent launch, stream-ordered scratch) is captured once in a CUDA graph
@@ -234,19 +235,29 @@ def time_chunkwise(w, steps, warmup, dev, flush, seed=0):
     B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
     q, k, v = (x.to(dev) for x in inputs.qkv(B, H, N, dk, dv, seed, torch.bfloat16))
     g = binding.gamma_schedule(H).to(dev)
-    out = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
     st = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if norm:
+        out = torch.empty(B, N, H, dv, dtype=torch.bfloat16, device=dev)
+        gw = torch.Generator().manual_seed(seed + 1)
+        wt, bs = torch.randn(H * dv, generator=gw).to(dev), torch.randn(H * dv, generator=gw).to(dev)
+
+        def call(s=None):
+            binding.retention_chunkwise_groupnorm(q, k, v, g, C, wt, bs, 1e-6, out=out, state_out=st, stream=s)
+    else:
+        out = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
+
+        def call(s=None):
+            binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st, stream=s)
     for _ in range(max(1, warmup)):
         flush.zero_()
-        binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
+        call()
     torch.cuda.synchronize(dev)
     graph = None
     try:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st,
-                                        stream=torch.cuda.current_stream(dev))
+            call(torch.cuda.current_stream(dev))
         for _ in range(warmup):
             flush.zero_()
             graph.replay()
@@ -259,7 +270,7 @@ def time_chunkwise(w, steps, warmup, dev, flush, seed=0):
         if graph is not None:
             graph.replay()
         else:
-            binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st)
+            call()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
@@ -495,6 +506,15 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(rbytes / rt / 1e9, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(rbytes / rt / 1e9 / hbm, 4), "traffic": None},
             "gpu_launches": 1}
+        # chunkwise with the GroupNorm fused into its epilogue, on the mid workload
+        tf, nf, _ = time_chunkwise(w, args.steps, 3, dev, flush, norm=True)
+        f_s = statistics.median(tf) / 1e3
+        extra["mid_groupnorm_fused"] = {
+            "tokens_per_s": round(w["B"] * w["N"] / f_s, 1), "ms_per_call": round(f_s * 1e3, 5),
+            "separate_ms": round(ms + gt * 1e3, 5),
+            "config": {"workload": "mid retention chunkwise fwd + GroupNorm over each head (fused epilogue)",
+                       "out_layout": "[B, N, H, dv]"},
+            "gpu_launches": nf}
         for wl in (LONG, B7):
             t, n, _ = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
             a_s = statistics.median(t) / 1e3

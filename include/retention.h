@@ -151,6 +151,31 @@ int retention_groupnorm(const void *r, const float *weight, const float *bias, v
                         int B, int H, int N, int dv, float eps, void *stream);
 
 /*
+ * retention_chunkwise_groupnorm -- retention_chunkwise with the normalisation
+ * of multi-scale retention fused into its output epilogue: "1. The Parallel
+ * Representation for High-Throughput Pretraining", MSR(X) =
+ * GroupNorm(Concat(R_1, ..., R_H)) W_O, one group per head ("1. PyTorch
+ * Implementation of MultiScaleRetention").  `out` receives, with the heads
+ * concatenated per token ([B][N][H][dv] bf16, the layout of
+ * retention_groupnorm's y),
+ *
+ *   out[b][n][h][c] = (R[c] - mu) / sqrt(var + eps) * weight[h dv + c] + bias[h dv + c]
+ *
+ * where R is the fp32 retention output row of (b, h, n) (before any bf16
+ * rounding) and mu, var its mean and biased variance over the dv channels.
+ * weight, bias: float32 [H dv], 16-byte aligned device memory, or NULL (one,
+ * zero).  eps >= 0.  state_out as for retention_chunkwise (the plain state).
+ * Supported when dv is 64 or 128 (a head's row is then one value tile of one
+ * CTA), with the chunk sizes and dk of retention_chunkwise; otherwise
+ * RET_ERR_UNSUPPORTED (use retention_chunkwise then retention_groupnorm).
+ * Workspace as for retention_chunkwise.
+ */
+int retention_chunkwise_groupnorm(const void *q, const void *k, const void *v, const float *gamma,
+                                  const float *weight, const float *bias, float eps,
+                                  void *out, float *state_out,
+                                  int B, int H, int N, int dk, int dv, int chunk, void *stream);
+
+/*
  * retention_chunkwise_workspace_size -- bytes of scratch retention_chunkwise_ws
  * needs for this shape (0 when the plan does not split the sequence).
  * Host only; returns RET_ERR_INVALID / RET_ERR_UNSUPPORTED like

@@ -34,6 +34,8 @@ _fp = ctypes.POINTER(ctypes.c_float)
 _SIGNATURES = {
     "retention_chunkwise": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_chunkwise_from_state": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+    "retention_chunkwise_groupnorm": [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _i, _i, _i, _i, _i,
+                                      _i, _vp],
     "retention_chunkwise_ws": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                ctypes.c_size_t, _vp],
     "retention_chunkwise_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
@@ -167,6 +169,32 @@ def retention_chunkwise_from_state(q, k, v, gamma, chunk: int, state_in, out=Non
     args = args[:4] + [_p(state_in)] + args[4:]
     _check("retention_chunkwise_from_state",
            lib().retention_chunkwise_from_state(*args, _stream(stream)))
+    return out, state_out
+
+
+def retention_chunkwise_groupnorm(q, k, v, gamma, chunk: int, weight=None, bias=None, eps: float = 1e-6,
+                                  out=None, state_out=None, want_state: bool = True, stream=None):
+    """bf16 chunkwise forward with the per-(token, head) GroupNorm fused into its
+    epilogue; returns (y [B, N, H, dv], state_out or None)."""
+    B, H, N, dk, dv = _seq_dims(q, v)
+    _need(q, "q", torch.bfloat16, (B, H, N, dk))
+    _need(k, "k", torch.bfloat16, (B, H, N, dk))
+    _need(v, "v", torch.bfloat16, (B, H, N, dv))
+    _need(gamma, "gamma", torch.float32, (H,))
+    for t, name in ((weight, "weight"), (bias, "bias")):
+        if t is not None:
+            _need(t, name, torch.float32, (H * dv,))
+    if out is None:
+        out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, N, H, dv))
+    if state_out is None and want_state:
+        state_out = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if state_out is not None:
+        _need(state_out, "state_out", torch.float32, (B, H, dk, dv))
+    _check("retention_chunkwise_groupnorm",
+           lib().retention_chunkwise_groupnorm(_p(q), _p(k), _p(v), _p(gamma), _p(weight), _p(bias), float(eps),
+                                               _p(out), _p(state_out), B, H, N, dk, dv, int(chunk),
+                                               _stream(stream)))
     return out, state_out
 
 

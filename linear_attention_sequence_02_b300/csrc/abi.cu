@@ -67,7 +67,7 @@ int plan_chunkwise(int B, int H, int N, int dk, int dv, int chunk, int sms, ret:
 // stream-ordered (cudaMallocAsync / cudaFreeAsync on the call's stream).
 int chunkwise_alloc(const void* q, const void* k, const void* v, const float* gamma,
                     const float* state_in, void* out, float* state_out, int B, int H, int N, int dk,
-                    int dv, int chunk, void* stream) {
+                    int dv, int chunk, const ret::ChunkNorm* norm, void* stream) {
   int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
   if (st != RET_OK) return st;
   ret::ChunkPlan plan;
@@ -75,6 +75,7 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
   if (sms <= 0) return RET_ERR_CUDA;
   st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
   if (st != RET_OK) return st;
+  if (norm && plan.n_dv_tiles != 1) return RET_ERR_UNSUPPORTED;  // a head's row must fit one CTA
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) {
     // the state after no tokens is the state before them
@@ -89,7 +90,7 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
       return RET_ERR_CUDA;
   }
   cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv,
-                                       chunk, plan, ws, s);
+                                       chunk, plan, ws, norm, s);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = e2;
@@ -167,20 +168,30 @@ int retention_chunkwise_ws(const void* q, const void* k, const void* v, const fl
       return RET_ERR_INVALID;
   }
   return from_cuda(ret::launch_chunk_tc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv,
-                                        chunk, plan, static_cast<float*>(workspace), s));
+                                        chunk, plan, static_cast<float*>(workspace), nullptr, s));
 }
 
 int retention_chunkwise(const void* q, const void* k, const void* v, const float* gamma, void* out,
                         float* state_out, int B, int H, int N, int dk, int dv, int chunk,
                         void* stream) {
-  return chunkwise_alloc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv, chunk, stream);
+  return chunkwise_alloc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream);
 }
 
 int retention_chunkwise_from_state(const void* q, const void* k, const void* v, const float* gamma,
                                    const float* state_in, void* out, float* state_out, int B, int H,
                                    int N, int dk, int dv, int chunk, void* stream) {
   if (state_in && (!aligned(state_in, 16) || state_in == state_out)) return RET_ERR_INVALID;
-  return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, stream);
+  return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream);
+}
+
+int retention_chunkwise_groupnorm(const void* q, const void* k, const void* v, const float* gamma,
+                                  const float* weight, const float* bias, float eps, void* out,
+                                  float* state_out, int B, int H, int N, int dk, int dv, int chunk,
+                                  void* stream) {
+  if (!(eps >= 0.f) || eps > 1e30f) return RET_ERR_INVALID;  // also rejects NaN
+  if ((weight && !aligned(weight, 16)) || (bias && !aligned(bias, 16))) return RET_ERR_INVALID;
+  const ret::ChunkNorm norm{weight, bias, eps};
+  return chunkwise_alloc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv, chunk, &norm, stream);
 }
 
 int retention_chunkwise_f32(const float* q, const float* k, const float* v, const float* gamma,

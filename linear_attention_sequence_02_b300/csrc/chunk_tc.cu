@@ -178,6 +178,9 @@ struct TcParams {
   const float* state_in;  // state before the first token, [B*H][DK][dv] (null: zero)
   float* state_out;  // main pass: final state (may be null)
   float* ws;         // segment states [B*H][segments-1][DK][dv]
+  const float* norm_w;  // GroupNorm of the outputs (NORM kernels): weight, bias [H dv]
+  const float* norm_b;  //   (null: one, zero) and eps
+  float norm_eps;
   int H, N, dv, n_dv_tiles, BH, segments, seg_chunks, n_chunks;
   float scale;       // 1/sqrt(dk)
 };
@@ -399,7 +402,7 @@ struct RoleCtx {
 // The four roles of a CTA (producer, MMA issuer, state group, output group).
 // FAST selects the rescaled form; a CTA picks one instantiation at its start,
 // so the code it runs holds no branches of the other form.
-template <int C, int DK, int DVT, bool SO, bool FAST>
+template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM>
 __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x) {
   using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
@@ -956,6 +959,30 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       const int vs = i % NV;
       uint8_t* stg = L::kSepStage ? sm + L::oStg : sm + L::oV + vs * L::kV;
       const uint32_t tO = tmem + lane_addr + L::cO + ob * DVT;
+      // GroupNorm of the row (NORM kernels; the row is the head's dv = DVT
+      // channels): first pass for its mean and variance, from sums shifted by
+      // the row's first value (no cancellation when the mean is large)
+      float mu = 0.f, inv = 0.f;
+      if constexpr (NORM) {
+        float x0 = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll 1
+        for (int cb = 0; cb < DVT / 32; cb += 2) {
+          uint32_t r[64];
+          tmem_ld32p(tO + cb * 32, &r[0]);
+          tmem_ld32p(tO + cb * 32 + 32, &r[32]);
+          tmem_wait_ld();
+          if (cb == 0) x0 = rt * __uint_as_float(r[0]);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const float d = fmaf(rt, __uint_as_float(r[j]), -x0);
+            s1 += d;
+            s2 = fmaf(d, d, s2);
+          }
+        }
+        const float m1 = s1 * (1.f / DVT);
+        mu = x0 + m1;
+        inv = rsqrtf(fmaxf(fmaf(-m1, m1, s2 * (1.f / DVT)), 0.f) + p.norm_eps);
+      }
 #pragma unroll 1
       for (int cb = 0; cb < DVT / 32; cb += 2) {
         uint32_t r[64];
@@ -974,9 +1001,27 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         }
         if (arow >= 0) {
           uint32_t pk[32];
+          if constexpr (NORM) {
+            // (o - mu) / sqrt(var + eps) * weight + bias, channel h dv + c
+            const int c0 = head * p.dv + cb * 32;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            pk[j] = pack_bf16(rt * __uint_as_float(r[2 * j]), rt * __uint_as_float(r[2 * j + 1]));
+            for (int q4 = 0; q4 < 16; ++q4) {
+              const float4 w = p.norm_w ? __ldg(reinterpret_cast<const float4*>(p.norm_w + c0) + q4)
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+              const float4 bb = p.norm_b ? __ldg(reinterpret_cast<const float4*>(p.norm_b + c0) + q4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float y0 = fmaf(fmaf(rt, __uint_as_float(r[4 * q4]), -mu) * inv, w.x, bb.x);
+              const float y1 = fmaf(fmaf(rt, __uint_as_float(r[4 * q4 + 1]), -mu) * inv, w.y, bb.y);
+              const float y2 = fmaf(fmaf(rt, __uint_as_float(r[4 * q4 + 2]), -mu) * inv, w.z, bb.z);
+              const float y3 = fmaf(fmaf(rt, __uint_as_float(r[4 * q4 + 3]), -mu) * inv, w.w, bb.w);
+              pk[2 * q4] = pack_bf16(y0, y1);
+              pk[2 * q4 + 1] = pack_bf16(y2, y3);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              pk[j] = pack_bf16(rt * __uint_as_float(r[2 * j]), rt * __uint_as_float(r[2 * j + 1]));
+          }
           store_row32_packed(stg, C, arow, cb * 32, &pk[0]);
           store_row32_packed(stg, C, arow, cb * 32 + 32, &pk[16]);
         }
@@ -986,8 +1031,12 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       if (eo == 0) {
         const int row0 = (c_begin + i) * C;
 #pragma unroll
-        for (int b = 0; b < DVT / 64; ++b)
-          tma_store_3d(x.tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, row0, bh);
+        for (int b = 0; b < DVT / 64; ++b) {
+          if constexpr (NORM)  // [B][N][H][dv]: (channel, head, token, batch row)
+            tma_store_4d(x.tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, head, row0, bh / p.H);
+          else
+            tma_store_3d(x.tmo, smem_u32(stg) + b * C * 128, dv0 + b * 64, row0, bh);
+        }
         bulk_commit_group();
         if (!L::kSepStage) {
           bulk_wait_group_read0();  // the V slot may be reloaded once the store has read it
@@ -1019,7 +1068,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
 
 }
 
-template <int C, int DK, int DVT, bool SO>
+template <int C, int DK, int DVT, bool SO, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -1095,8 +1144,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   if (SO) griddep_launch_dependents();
 
   const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC};
-  if (fast) chunk_roles<C, DK, DVT, SO, true>(p, x);
-  else chunk_roles<C, DK, DVT, SO, false>(p, x);
+  if (fast) chunk_roles<C, DK, DVT, SO, true, NORM>(p, x);
+  else chunk_roles<C, DK, DVT, SO, false, NORM>(p, x);
 
   // ---- teardown: every MMA has completed, every load landed, every store read ----
   tc_fence_before();
@@ -1147,11 +1196,27 @@ bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows) 
   return r == CUDA_SUCCESS;
 }
 
-template <int C, int DK, int DVT, bool SO>
+// [B][N][H][dv] bf16 outputs (heads concatenated per token) viewed in 4-D as
+// (channel, head, token, batch row), boxes of 64 channels x 1 head x `rows`
+// tokens, 128-byte swizzle: one CTA's tile of one head.
+bool make_map_heads(CUtensorMap* m, const void* base, int dv, int H, int N, int B, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)dv, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)dv * 2, (cuuint64_t)dv * 2 * H, (cuuint64_t)dv * 2 * H * (cuuint64_t)N};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int C, int DK, int DVT, bool SO, bool NORM>
 cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mo, const TcParams& p, int grid, bool pdl, cudaStream_t s) {
   using L = Cfg<C, DK, DVT, SO>;
-  auto kern = chunk_tc_kernel<C, DK, DVT, SO>;
+  auto kern = chunk_tc_kernel<C, DK, DVT, SO, NORM>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -1180,16 +1245,16 @@ cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return cudaGetLastError();
 }
 
-template <int C, int DK, int DVT>
+template <int C, int DK, int DVT, bool NORM>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   const bool split = p.segments > 1;
   if (split) {
-    cudaError_t e = launch_one<C, DK, DVT, true>(mq, mk, mv, mo, p, p.BH * (p.segments - 1) * p.n_dv_tiles,
+    cudaError_t e = launch_one<C, DK, DVT, true, false>(mq, mk, mv, mo, p, p.BH * (p.segments - 1) * p.n_dv_tiles,
                                                  false, s);
     if (e != cudaSuccess) return e;
   }
-  return launch_one<C, DK, DVT, false>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
+  return launch_one<C, DK, DVT, false, NORM>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
 }
 
 // The value-tile width used for these sizes.
@@ -1225,18 +1290,23 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H, int N,
-                            int dk, int dv, int chunk,
-                            const ChunkPlan& plan, float* workspace, cudaStream_t s) {
+                            int dk, int dv, int chunk, const ChunkPlan& plan, float* workspace,
+                            const ChunkNorm* norm, cudaStream_t s) {
   const int BH = B * H;
+  if (norm && plan.n_dv_tiles != 1) return cudaErrorNotSupported;  // a row must fit one CTA
   CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, q, dk, N, BH, chunk) || !make_map(&mk, k, dk, N, BH, chunk) ||
-      !make_map(&mv, v, dv, N, BH, chunk) || !make_map(&mo, out, dv, N, BH, chunk))
+      !make_map(&mv, v, dv, N, BH, chunk) ||
+      !(norm ? make_map_heads(&mo, out, dv, H, N, B, chunk) : make_map(&mo, out, dv, N, BH, chunk)))
     return cudaErrorInvalidValue;
   TcParams p;
   p.gamma = gamma;
   p.state_in = state_in;
   p.state_out = state_out;
   p.ws = workspace;
+  p.norm_w = norm ? norm->weight : nullptr;
+  p.norm_b = norm ? norm->bias : nullptr;
+  p.norm_eps = norm ? norm->eps : 0.f;
   p.H = H;
   p.N = N;
   p.dv = dv;
@@ -1247,14 +1317,25 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.n_chunks = plan.n_chunks;
   p.scale = (float)(1.0 / std::sqrt((double)dk));
   const bool t128 = plan.dvt == 128;
-  if (chunk == 64 && dk == 128) return t128 ? launch_pair<64, 128, 128>(mq, mk, mv, mo, p, s)
-                                            : launch_pair<64, 128, 64>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dk == 128) return t128 ? launch_pair<128, 128, 128>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<128, 128, 64>(mq, mk, mv, mo, p, s);
-  if (chunk == 64 && dk == 256) return t128 ? launch_pair<64, 256, 128>(mq, mk, mv, mo, p, s)
-                                            : launch_pair<64, 256, 64>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dk == 256) return t128 ? launch_pair<128, 256, 128>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<128, 256, 64>(mq, mk, mv, mo, p, s);
+  if (norm) {
+    if (chunk == 64 && dk == 128) return t128 ? launch_pair<64, 128, 128, true>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<64, 128, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 128 && dk == 128) return t128 ? launch_pair<128, 128, 128, true>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<128, 128, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 64 && dk == 256) return t128 ? launch_pair<64, 256, 128, true>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<64, 256, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 128 && dk == 256) return t128 ? launch_pair<128, 256, 128, true>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<128, 256, 64, true>(mq, mk, mv, mo, p, s);
+    return cudaErrorNotSupported;
+  }
+  if (chunk == 64 && dk == 128) return t128 ? launch_pair<64, 128, 128, false>(mq, mk, mv, mo, p, s)
+                                            : launch_pair<64, 128, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dk == 128) return t128 ? launch_pair<128, 128, 128, false>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<128, 128, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dk == 256) return t128 ? launch_pair<64, 256, 128, false>(mq, mk, mv, mo, p, s)
+                                            : launch_pair<64, 256, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dk == 256) return t128 ? launch_pair<128, 256, 128, false>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<128, 256, 64, false>(mq, mk, mv, mo, p, s);
   return cudaErrorNotSupported;
 }
 

@@ -40,11 +40,20 @@ struct ChunkPlan {
 };
 // Fills `plan` for a supported shape; returns false for unsupported shapes.
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan);
-// state_in (nullable) is the state before the first token, [B*H][dk][dv].
+// GroupNorm of the outputs fused into the chunkwise epilogue (one value tile
+// per head): weight, bias [H dv] (nullable: one, zero) and eps; the outputs are
+// then written [B][N][H][dv].
+struct ChunkNorm {
+  const float* weight;
+  const float* bias;
+  float eps;
+};
+// state_in (nullable) is the state before the first token, [B*H][dk][dv];
+// norm (nullable) selects the GroupNorm epilogue.
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H,
                             int N, int dk, int dv, int chunk, const ChunkPlan& plan,
-                            float* workspace, cudaStream_t s);
+                            float* workspace, const ChunkNorm* norm, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 
 // ---- position phase rotation of queries and keys (rotate.cu) -------------------

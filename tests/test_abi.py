@@ -120,3 +120,12 @@ def test_rotate_validation(lib):
     assert rot(P, P, P, 1, 1, 4, 128, -1, None) == binding.RET_ERR_INVALID
     assert rot(P, P, P, 1, 1, 4, 124, 0, None) == binding.RET_ERR_UNSUPPORTED
     assert rot(P, P, P, 1, 1, 4, 128, (1 << 24) - 3, None) == binding.RET_ERR_UNSUPPORTED
+
+
+def test_chunkwise_groupnorm_validation(lib):
+    fn = lib.retention_chunkwise_groupnorm
+    # (q, k, v, gamma, weight, bias, eps, out, state_out, B, H, N, dk, dv, chunk, stream)
+    assert fn(P, P, P, P, None, None, -1.0, P, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
+    assert fn(P, P, P, P, ctypes.c_void_p(0x1008), None, 1e-6, P, None, 1, 1, 8, 128, 128, 64, None) == \
+        binding.RET_ERR_INVALID
+    assert fn(None, P, P, P, None, None, 1e-6, P, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
