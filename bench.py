@@ -4,7 +4,9 @@ Headline: chunkwise-forward tokens/s (B*N sequence positions per second, all
 heads included) on the mid workload B=4, H=8, N=2048, d_k=d_v=128, chunk=64,
 bf16 q/k/v/out with fp32 accumulation and state.  One step = one
 retention_chunkwise call over one batch; inputs are resident in HBM and L2 is
-flushed (a 512 MiB write) between timed steps, outside the timed events.
+flushed between timed steps, outside the timed events: a 512 MiB write, then
+a 512 MiB read, so that neither the inputs nor the flush's own dirty lines
+(whose write-back would land inside the timed call) remain in L2.
 
 Also reported on the same line:
   decode      the recurrent decode step on 64 sequences x 16 heads, d_k=128,
@@ -50,6 +52,21 @@ B7 = dict(name="7b", B=8, H=16, N=8192, dk=256, dv=512, chunk=128)
 DECODE = dict(name="decode", T=1024, B=64, H=16, dk=128, dv=256)
 METRIC = "retention tokens/s (chunkwise fwd, 1 B300) + decode steps/s; % of roofline"
 L2_FLUSH_BYTES = 512 << 20
+
+
+class L2Flush:
+    """Run between timed steps: writes a buffer larger than the 126 MB L2, then
+    reads another one, so that the timed call finds neither its inputs in L2
+    nor the flush's own dirty lines still waiting to be written back to DRAM."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.acc += self.r.sum()
 
 
 def peaks():
@@ -250,7 +267,7 @@ def time_chunkwise(w, steps, warmup, dev, flush, seed=0, norm=False):
         def call(s=None):
             binding.retention_chunkwise(q, k, v, g, C, out=out, state_out=st, stream=s)
     for _ in range(max(1, warmup)):
-        flush.zero_()
+        flush()
         call()
     torch.cuda.synchronize(dev)
     graph = None
@@ -259,7 +276,7 @@ def time_chunkwise(w, steps, warmup, dev, flush, seed=0, norm=False):
         with torch.cuda.graph(graph):
             call(torch.cuda.current_stream(dev))
         for _ in range(warmup):
-            flush.zero_()
+            flush()
             graph.replay()
         torch.cuda.synchronize(dev)
     except Exception:
@@ -275,7 +292,7 @@ def time_chunkwise(w, steps, warmup, dev, flush, seed=0, norm=False):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(stream)
         run()
         b.record(stream)
@@ -374,7 +391,7 @@ def time_groupnorm(w, reps, dev, flush, seed=0):
         binding.retention_groupnorm(r, wt, bs, 1e-6, out=y)
     times = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         binding.retention_groupnorm(r, wt, bs, 1e-6, out=y)
@@ -400,7 +417,7 @@ def time_rotate(w, reps, dev, flush, seed=0):
         binding.retention_rotate(x, th, 0, out=y)
     times = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         binding.retention_rotate(x, th, 0, out=y)
@@ -436,7 +453,7 @@ def run_ours(args):
     from linear_attention_sequence_02_b300 import binding
     binding.lib()
     hbm, tflops, peak_kind = peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     # ---- headline: mid chunkwise, device-timed ----
     w = MID
@@ -490,7 +507,7 @@ def run_ours(args):
         gbytes = 4 * gw["dv"] * rows  # bf16 row read + bf16 row written
         extra["groupnorm"] = {
             "rows_per_s": round(rows / gt, 1), "ms_per_call": round(gt * 1e3, 5),
-            "config": {k: gw[k] for k in ("B", "H", "N", "dv")} | {"l2": "flushed before each call",
+            "config": {k: gw[k] for k in ("B", "H", "N", "dv")} | {"l2": "flushed before each call (512 MiB write, then 512 MiB read)",
                                                                    "timing": "CUDA events per call"},
             "roofline": {"bound": "hbm", "achieved": round(gbytes / gt / 1e9, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbytes / gt / 1e9 / hbm, 4), "traffic": recorded_traffic("groupnorm")},
@@ -501,7 +518,7 @@ def run_ours(args):
         rbytes = 4 * rw["d"] * rrows  # bf16 row read + bf16 row written
         extra["rotate"] = {
             "rows_per_s": round(rrows / rt, 1), "ms_per_call": round(rt * 1e3, 5),
-            "config": {k: rw[k] for k in ("B", "H", "N", "d")} | {"l2": "flushed before each call",
+            "config": {k: rw[k] for k in ("B", "H", "N", "d")} | {"l2": "flushed before each call (512 MiB write, then 512 MiB read)",
                                                                   "timing": "CUDA events per call"},
             "roofline": {"bound": "hbm", "achieved": round(rbytes / rt / 1e9, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(rbytes / rt / 1e9 / hbm, 4), "traffic": None},
@@ -535,7 +552,7 @@ def run_ours(args):
         "config": {"workload": "mid retention chunkwise fwd", "B": w["B"], "H": w["H"], "N": w["N"],
                    "dk": w["dk"], "dv": w["dv"], "chunk": w["chunk"], "global_batch": w["B"] * world,
                    "seq_len": w["N"], "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": "flushed (512 MiB write) between timed steps",
+                   "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)",
                    "timing": how},
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -596,7 +613,7 @@ def run_only(args):
         t = time_decode(DECODE, args.steps, dev)
         print(json.dumps({"only": "decode", "ms_per_step": statistics.median(t)}))
         return
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     if args.only in ("groupnorm", "rotate"):
         fn, wl = (time_groupnorm, GROUPNORM) if args.only == "groupnorm" else (time_rotate, ROTATE)
         t = fn(wl, args.steps, dev, flush)
