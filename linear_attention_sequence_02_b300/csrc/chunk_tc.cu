@@ -38,19 +38,23 @@
 //                   state update (every MMA of the state-only pre-pass)
 //   warp 10 lane 0: issues Q S and P~ W, the products accumulated into O
 //   warps 2..5    : state group: W = diag(w) V in place, the bf16 snapshot of
-//                   the state for the Q S product, the initial and final states
+//                   the state for the Q S product, the final state; with the
+//                   output group, the initial state of a later segment
 //   warps 6..9    : output group: causal mask of P = Q K^T into bf16 in place in
-//                   tensor memory (the A operand of P~ W), output rows scaled,
-//                   staged in the chunk's V slot and written by a TMA store
+//                   tensor memory (the A operand of P~ W); output rows scaled
+//                   (with NORM, normalised per head first), staged in shared
+//                   memory (its own buffer, or the chunk's V slot when there
+//                   is no room) and written by a TMA store
 // Warp w (w >= 2) reads TMEM lanes 32*(w%4) .. +31.
 //
 // Long sequences are cut into segments so that enough CTAs fill the GPU.  A
 // state-only pre-pass (this kernel with SO = true: K and V only) writes each
 // segment's local end state to a float32 workspace; the main pass starts
-// segment s from sum_{t<s} gamma^((s-1-t) Lseg) state_t.  The main pass is
-// launched with programmatic stream serialisation: its CTAs start while the
-// pre-pass runs and only the state group waits (griddepcontrol.wait) before it
-// reads the workspace.
+// segment s from gamma^(s Lseg) state_in (the caller's starting state, if any)
+// plus sum_{t<s} gamma^((s-1-t) Lseg) state_t.  The main pass is launched with
+// programmatic stream serialisation: its CTAs start while the pre-pass runs
+// and only the two epilogue groups of a later segment wait
+// (griddepcontrol.wait) before they read the workspace.
 //
 // Every mbarrier wait gives up after kWaitLimitNs, sets RET_DEV_WAIT_TIMEOUT in
 // the device status word and unwinds: in-flight TMA loads and MMAs are waited
