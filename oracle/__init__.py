@@ -1,7 +1,7 @@
 """fp64 CPU oracle for RetNet retention -- TEST INFRASTRUCTURE ONLY.
 
 Nothing in the product path imports this package.  It is loaded only by the
-test suite, by the smoke check (to judge one small GPU run) and by the
+test suite, by the smoke check (to check one small GPU run) and by the
 benchmark's CPU-baseline leg.  It shares no code with the CUDA library: the
 arithmetic lives in ``retention_oracle.c`` (plain C, fp64, one OpenMP loop over
 heads) and this module only compiles that file with gcc and marshals numpy
