@@ -16,6 +16,10 @@ Functions (see the C file for the formulas and the page sections they follow):
   groupnorm(r, weight=None, bias=None, eps=1e-6)  per-(token, head)
                                normalisation, heads concatenated per token
   rotate(x, theta, n0=0)       position phase rotation of queries or keys
+  backward(q, k, v, gamma, dout, dstate=None, state_in=None)
+                               gradients of the forward (with optional
+                               starting state) for output and final-state
+                               gradients; returns (dq, dk, dv, dstate_in)
 
 Every function here is pinned by tests/test_oracle.py against closed forms,
 hand-expanded sums, a library-routine special case and the three-form
@@ -92,6 +96,8 @@ class Oracle:
         lib.oracle_rotate.argtypes = [_dp, _dp, _dp] + [ctypes.c_int] * 4 + [ctypes.c_long]
         lib.oracle_groupnorm.restype = None
         lib.oracle_groupnorm.argtypes = [_dp, _dp, _dp, _dp] + [ctypes.c_int] * 4 + [ctypes.c_double]
+        lib.oracle_backward.restype = None
+        lib.oracle_backward.argtypes = [_dp] * 11 + [ctypes.c_int] * 5
         self.lib = lib
 
     def threads(self) -> int:
@@ -171,6 +177,24 @@ class Oracle:
         self.lib.oracle_rotate(_ptr(x), _ptr(th), _ptr(y), B, H, N, d, int(n0))
         return y
 
+    def backward(self, q, k, v, gammas, dout, dstate=None, state_in=None):
+        """Gradients of sum(dout * out) + sum(dstate * S_N) with respect to q,
+        k, v and the starting state, for the forward started from state_in
+        (zero if None).  Returns (dq, dk, dv, dstate_in), all fp64."""
+        q, k, v, g, do = _f64(q), _f64(k), _f64(v), _f64(gammas), _f64(dout)
+        B, H, N, dk, dv = _dims(q, v)
+        s0 = None if state_in is None else _f64(state_in)
+        ds = None if dstate is None else _f64(dstate)
+        dq = np.zeros((B, H, N, dk), dtype=np.float64)
+        dkk = np.zeros((B, H, N, dk), dtype=np.float64)
+        dvv = np.zeros((B, H, N, dv), dtype=np.float64)
+        ds0 = np.zeros((B, H, dk, dv), dtype=np.float64)
+        self.lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 None if s0 is None else _ptr(s0), _ptr(do),
+                                 None if ds is None else _ptr(ds),
+                                 _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(ds0), B, H, N, dk, dv)
+        return dq, dkk, dvv, ds0
+
 
 def default() -> Oracle:
     """The oracle compiled from retention_oracle.c beside this file."""
@@ -211,3 +235,7 @@ def groupnorm(r, weight=None, bias=None, eps=1e-6):
 
 def rotate(x, theta, n0=0):
     return default().rotate(x, theta, n0)
+
+
+def backward(q, k, v, gammas, dout, dstate=None, state_in=None):
+    return default().backward(q, k, v, gammas, dout, dstate, state_in)

@@ -308,3 +308,102 @@ void oracle_rotate(const double *x, const double *theta, double *y, int B, int H
         }
       }
 }
+
+/*
+ * Backward pass.  The pages say the chunkwise form exists so that long
+ * sequences can be trained ([G] "3. The Chunkwise Recurrent Representation
+ * ..."), but print no gradient; the oracle therefore differentiates the
+ * definition, written with a starting state S0 (readings R2, R5):
+ *
+ *   out_n = s sum_{m<=n} g^(n-m) (q_n . k_m) v_m  +  s g^(n+1) q_n S0
+ *   S_N   = g^N S0 + sum_m g^(N-1-m) k_m^T v_m          (s = 1/sqrt(dk))
+ *
+ * For the loss sum_n dout_n . out_n + <dS, S_N> (dout: [N][dv], dS: [dk][dv])
+ * the partial derivatives are
+ *
+ *   dq_n  = s sum_{m<=n} g^(n-m) (dout_n . v_m) k_m   +  s g^(n+1) S0 dout_n
+ *   dk_m  = s sum_{n>=m} g^(n-m) (dout_n . v_m) q_n   +  g^(N-1-m) dS v_m
+ *   dv_m  = s sum_{n>=m} g^(n-m) (q_n . k_m) dout_n   +  g^(N-1-m) k_m dS
+ *   dS0   = s sum_n g^(n+1) q_n^T dout_n              +  g^N dS
+ *
+ * (S0 dout_n and dS v_m are [dk][dv] x [dv] products; k_m dS is [dk] x
+ * [dk][dv].)  state_in (S0), dstate (dS) and dstate_in (dS0) are
+ * [B][H][dk][dv] and may be NULL: a NULL S0 or dS is zero, a NULL dstate_in is
+ * not written.  dq, dk: [B][H][N][dk]; dv_out: [B][H][N][dv].
+ */
+void oracle_backward(const double *q, const double *k, const double *v,
+                     const double *gamma, const double *state_in,
+                     const double *dout, const double *dstate,
+                     double *dq, double *dk_out, double *dv_out, double *dstate_in,
+                     int B, int H, int N, int dk, int dv)
+{
+    const double scale = 1.0 / sqrt((double)dk);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            const size_t head = (size_t)b * H + h;
+            const double *Q = q + head * (size_t)N * dk;
+            const double *K = k + head * (size_t)N * dk;
+            const double *V = v + head * (size_t)N * dv;
+            const double *dO = dout + head * (size_t)N * dv;
+            const double *S0 = state_in ? state_in + head * (size_t)dk * dv : NULL;
+            const double *dS = dstate ? dstate + head * (size_t)dk * dv : NULL;
+            double *dQ = dq + head * (size_t)N * dk;
+            double *dK = dk_out + head * (size_t)N * dk;
+            double *dV = dv_out + head * (size_t)N * dv;
+            const double g = gamma[h];
+
+            /* dq_n: causal sum over m <= n, then the starting-state term */
+            for (int n = 0; n < N; ++n) {
+                double *r = dQ + (size_t)n * dk;
+                for (int i = 0; i < dk; ++i) r[i] = 0.0;
+                for (int m = 0; m <= n; ++m) {
+                    const double w = scale * pow(g, (double)(n - m)) *
+                                     dot(dO + (size_t)n * dv, V + (size_t)m * dv, dv);
+                    for (int i = 0; i < dk; ++i) r[i] += w * K[(size_t)m * dk + i];
+                }
+                if (S0) {
+                    const double z = scale * pow(g, (double)(n + 1));
+                    for (int i = 0; i < dk; ++i)
+                        r[i] += z * dot(S0 + (size_t)i * dv, dO + (size_t)n * dv, dv);
+                }
+            }
+            /* dk_m and dv_m: anti-causal sums over n >= m, then the final-state term */
+            for (int m = 0; m < N; ++m) {
+                double *rk = dK + (size_t)m * dk;
+                double *rv = dV + (size_t)m * dv;
+                for (int i = 0; i < dk; ++i) rk[i] = 0.0;
+                for (int c = 0; c < dv; ++c) rv[c] = 0.0;
+                for (int n = m; n < N; ++n) {
+                    const double d = scale * pow(g, (double)(n - m));
+                    const double wk = d * dot(dO + (size_t)n * dv, V + (size_t)m * dv, dv);
+                    const double wv = d * dot(Q + (size_t)n * dk, K + (size_t)m * dk, dk);
+                    for (int i = 0; i < dk; ++i) rk[i] += wk * Q[(size_t)n * dk + i];
+                    for (int c = 0; c < dv; ++c) rv[c] += wv * dO[(size_t)n * dv + c];
+                }
+                if (dS) {
+                    const double xi = pow(g, (double)(N - 1 - m));
+                    for (int i = 0; i < dk; ++i)
+                        rk[i] += xi * dot(dS + (size_t)i * dv, V + (size_t)m * dv, dv);
+                    for (int c = 0; c < dv; ++c) {
+                        double t = 0.0;
+                        for (int i = 0; i < dk; ++i) t += K[(size_t)m * dk + i] * dS[(size_t)i * dv + c];
+                        rv[c] += xi * t;
+                    }
+                }
+            }
+            /* dS0 = s sum_n g^(n+1) q_n^T dout_n + g^N dS */
+            if (dstate_in) {
+                double *r = dstate_in + head * (size_t)dk * dv;
+                for (int i = 0; i < dk; ++i)
+                    for (int c = 0; c < dv; ++c) {
+                        double t = dS ? pow(g, (double)N) * dS[(size_t)i * dv + c] : 0.0;
+                        for (int n = 0; n < N; ++n)
+                            t += scale * pow(g, (double)(n + 1)) * Q[(size_t)n * dk + i] *
+                                 dO[(size_t)n * dv + c];
+                        r[(size_t)i * dv + c] = t;
+                    }
+            }
+        }
+    }
+}

@@ -326,6 +326,110 @@ def check_rotation_special_cases(o):
     _close(o.rotate(o.rotate(x1, th, 3), th, 4), o.rotate(x1, th, 7), 1e-13, "rotations compose")
 
 
+# --- the backward pass -------------------------------------------------------------
+
+def _loss(o, q, k, v, g, dout, dstate, state_in):
+    """sum(dout * out) + sum(dstate * S_N) for the forward from state_in."""
+    out, S = o.recurrent(q, k, v, g, state=state_in)
+    return float(np.sum(dout * out) + (0.0 if dstate is None else np.sum(dstate * S)))
+
+
+def check_backward_hand_expanded(o):
+    gold = _read_golden("backward_hand_n2.txt")
+    sh = (1, 1, 2, 1)
+    q, k, v, dout = (gold[x].reshape(sh) for x in ("q", "k", "v", "dout"))
+    S0, dS = gold["state_in"].reshape(1, 1, 1, 1), gold["dstate"].reshape(1, 1, 1, 1)
+    dq, dk, dv, ds0 = o.backward(q, k, v, gold["gamma"], dout, dS, S0)
+    assert np.array_equal(dq.ravel(), gold["dq"]), dq.ravel()
+    assert np.array_equal(dk.ravel(), gold["dk"]), dk.ravel()
+    assert np.array_equal(dv.ravel(), gold["dv"]), dv.ravel()
+    assert np.array_equal(ds0.ravel(), gold["dstate_in"]), ds0.ravel()
+
+
+def check_backward_is_the_derivative(o):
+    """The forward is linear in each of q, k, v and the starting state, so
+    L(x + e) - L(x) equals <dL/dx, e> exactly up to rounding for any e: checked
+    for random directions, with and without a starting state and a final-state
+    gradient, for decays 0.9, 0.5, 0 and 1."""
+    B, H, N, dk, dv = 2, 4, 13, 5, 3
+    g = np.array([0.9, 0.5, 0.0, 1.0])
+    q, k, v = _rand((B, H, N, dk), 80), _rand((B, H, N, dk), 81), _rand((B, H, N, dv), 82)
+    dout, S0, dS = _rand((B, H, N, dv), 83), _rand((B, H, dk, dv), 84), _rand((B, H, dk, dv), 85)
+    for s0, ds in ((S0, dS), (None, None), (S0, None), (None, dS)):
+        grads = o.backward(q, k, v, g, dout, ds, s0)
+        base = _loss(o, q, k, v, g, dout, ds, s0)
+        args = [q, k, v, np.zeros((B, H, dk, dv)) if s0 is None else s0]
+        for which, grad in enumerate(grads):
+            e = _rand(args[which].shape, 90 + which)
+            moved = list(args)
+            moved[which] = args[which] + e
+            got = _loss(o, *moved[:3], g, dout, ds, moved[3]) - base
+            want = float(np.sum(grad * e))
+            assert abs(got - want) <= 1e-11 * max(1.0, abs(want)), (which, got, want)
+
+
+def check_backward_brute_force_tiny(o):
+    """Every entry of every gradient, one unit direction at a time (N = 3,
+    d_k = d_v = 2, starting state and final-state gradient present)."""
+    B, H, N, dk, dv = 1, 1, 3, 2, 2
+    g = np.array([0.75])
+    q, k, v = _rand((B, H, N, dk), 86), _rand((B, H, N, dk), 87), _rand((B, H, N, dv), 88)
+    dout, S0, dS = _rand((B, H, N, dv), 89), _rand((B, H, dk, dv), 90), _rand((B, H, dk, dv), 91)
+    grads = o.backward(q, k, v, g, dout, dS, S0)
+    base = _loss(o, q, k, v, g, dout, dS, S0)
+    args = [q, k, v, S0]
+    for which, grad in enumerate(grads):
+        for idx in np.ndindex(*args[which].shape):
+            moved = [a.copy() for a in args]
+            moved[which][idx] += 1.0
+            got = _loss(o, *moved[:3], g, dout, dS, moved[3]) - base
+            assert abs(got - grad[idx]) <= 1e-12 * max(1.0, abs(got)), (which, idx, got, grad[idx])
+
+
+def check_backward_euler_identities(o):
+    """out is linear in q, and out and S_N are jointly linear in (k, S0) and in
+    (v, S0), so <dq, q> = <dout, out> and <dk, k> + <dS0, S0> = <dv, v> +
+    <dS0, S0> = L; these hold at any size."""
+    B, H, N, dk, dv = 1, 3, 40, 8, 6
+    g = np.array([0.96875, 0.7, 0.2])
+    q, k, v = _rand((B, H, N, dk), 92), _rand((B, H, N, dk), 93), _rand((B, H, N, dv), 94)
+    dout, S0, dS = _rand((B, H, N, dv), 95), _rand((B, H, dk, dv), 96), _rand((B, H, dk, dv), 97)
+    out, S = o.recurrent(q, k, v, g, state=S0)
+    dq, dk_, dv_, ds0 = o.backward(q, k, v, g, dout, dS, S0)
+    lo, L = np.sum(dout * out), np.sum(dout * out) + np.sum(dS * S)
+    _close(np.sum(dq * q), lo, 1e-13, "<dq, q>")
+    _close(np.sum(dk_ * k) + np.sum(ds0 * S0), L, 1e-13, "<dk, k> + <dS0, S0>")
+    _close(np.sum(dv_ * v) + np.sum(ds0 * S0), L, 1e-13, "<dv, v> + <dS0, S0>")
+
+
+def check_backward_gamma_one_is_library_autograd(o):
+    """With gamma = 1 and no states the forward is tril(Q K^T) V / sqrt(d_k), so
+    its gradients are those torch's autograd gives for that product (fp64)."""
+    import torch
+    B, H, N, dk, dv = 1, 2, 17, 4, 3
+    q, k, v = _rand((B, H, N, dk), 98), _rand((B, H, N, dk), 99), _rand((B, H, N, dv), 100)
+    dout = _rand((B, H, N, dv), 101)
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_(True) for x in (q, k, v))
+    out = torch.tril(tq @ tk.transpose(-1, -2)) @ tv / math.sqrt(dk)
+    out.backward(torch.from_numpy(dout))
+    dq, dk_, dv_, ds0 = o.backward(q, k, v, np.ones(H), dout)
+    _close(dq, tq.grad.numpy(), 1e-13, "dq vs autograd")
+    _close(dk_, tk.grad.numpy(), 1e-13, "dk vs autograd")
+    _close(dv_, tv.grad.numpy(), 1e-13, "dv vs autograd")
+    want_ds0 = np.einsum("bhnk,bhnv->bhkv", q, dout) / math.sqrt(dk)
+    _close(ds0, want_ds0, 1e-13, "dS0 at gamma = 1")
+
+
+def check_backward_empty_sequence(o):
+    """N = 0: no gradients of the sequence; the starting state's gradient is dS."""
+    q = np.zeros((1, 2, 0, 4))
+    v = np.zeros((1, 2, 0, 3))
+    dS = _rand((1, 2, 4, 3), 102)
+    dq, dk, dv, ds0 = o.backward(q, q, v, np.array([0.9, 0.0]), v, dS)
+    assert dq.shape == (1, 2, 0, 4) and dv.shape == (1, 2, 0, 3)
+    assert np.array_equal(ds0, dS)
+
+
 ALL_CHECKS = [
     check_gamma_printed,
     check_hand_expanded_scalar,
@@ -343,4 +447,10 @@ ALL_CHECKS = [
     check_groupnorm_invariants,
     check_rotation_relative_position,
     check_rotation_special_cases,
+    check_backward_hand_expanded,
+    check_backward_is_the_derivative,
+    check_backward_brute_force_tiny,
+    check_backward_euler_identities,
+    check_backward_gamma_one_is_library_autograd,
+    check_backward_empty_sequence,
 ]

@@ -48,6 +48,20 @@ MUTANTS = {
                              "const double a = (double)n * theta[j];"),
     "rotate_pairs_split": ("yr[2 * j + 1] = xr[2 * j] * s + xr[2 * j + 1] * c;",
                            "yr[2 * j + 1] = xr[(2 * j + 2) % d] * s + xr[2 * j + 1] * c;"),
+    "bwd_dq_zeta_off_by_one": ("const double z = scale * pow(g, (double)(n + 1));",
+                               "const double z = scale * pow(g, (double)n);"),
+    "bwd_dq_decay_off_by_one": ("const double w = scale * pow(g, (double)(n - m)) *",
+                                "const double w = scale * pow(g, (double)(n - m + 1)) *"),
+    "bwd_dk_final_state_term_dropped": ("rk[i] += xi * dot(dS + (size_t)i * dv, V + (size_t)m * dv, dv);",
+                                        "rk[i] += 0.0 * xi;"),
+    "bwd_dv_scores_transposed": ("const double wv = d * dot(Q + (size_t)n * dk, K + (size_t)m * dk, dk);",
+                                 "const double wv = d * dot(Q + (size_t)m * dk, K + (size_t)n * dk, dk);"),
+    "bwd_no_scale_on_key_value_grads": ("const double d = scale * pow(g, (double)(n - m));",
+                                        "const double d = pow(g, (double)(n - m));"),
+    "bwd_ds0_no_decay_of_ds": ("double t = dS ? pow(g, (double)N) * dS[(size_t)i * dv + c] : 0.0;",
+                               "double t = dS ? dS[(size_t)i * dv + c] : 0.0;"),
+    "bwd_dv_final_state_transposed": ("for (int i = 0; i < dk; ++i) t += K[(size_t)m * dk + i] * dS[(size_t)i * dv + c];",
+                                      "for (int i = 0; i < dk; ++i) t += K[(size_t)m * dk + i] * dS[(size_t)((i + c) % dk) * dv + c];"),
 }
 
 
