@@ -24,7 +24,7 @@ Also reported on the same line:
 
 `--impl reference` times the fp64 CPU oracle alone on the same workload and
 metric (the full mid workload per step) and prints its own line.
-`--only {mid,long,7b,decode}` runs one workload alone and prints its timing
+`--only {mid,long,7b,decode,groupnorm,rotate,backward}` runs one workload alone and prints its timing
 (used to give ncu a small, single-workload command).
 Under torchrun each rank runs its own replica (independent batches, no
 collective on the data path); value = all ranks' tokens / max rank time.
@@ -427,6 +427,53 @@ def time_rotate(w, reps, dev, flush, seed=0):
     return times
 
 
+def backward_chunk(dk: int, dv: int) -> int:
+    """The chunk length the gradient kernel uses inside: 64 while both widths
+    are at most 256, else 32 (so its shared-memory tiles fit one CTA)."""
+    return 32 if max(dk, dv) > 256 else 64
+
+
+def backward_flops(w, C: int) -> int:
+    """Algorithmic flops of one gradient call at internal chunk C (causal part
+    only): per head-token the dq scan's scores, weighted rows, cross term and
+    state update, (C+1)(dk+dv) + 4 dk dv; the dk scan the same; the dv scan
+    its scores and rows, (C+1)(dk+dv), plus its cross term, 2 dk dv (the
+    state-gradient update is counted once, in the dk scan)."""
+    B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
+    return B * H * N * (3 * (C + 1) * (dk + dv) + 10 * dk * dv)
+
+
+def backward_bytes(w) -> int:
+    """Algorithmic HBM bytes of one gradient call without states: q, k, v and
+    dout read, dq, dk, dv written (bf16)."""
+    B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
+    return B * H * N * 2 * (2 * (2 * dk + dv) + dv)
+
+
+def time_backward(w, reps, dev, flush, seed=0):
+    """ms per retention_backward call (no starting state, no final-state
+    gradient: the usual training case) on the workload, L2 flushed first."""
+    from linear_attention_sequence_02_b300 import binding
+    B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
+    g = torch.Generator().manual_seed(seed)
+    q, k, v, do = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16).to(dev) for d in (dk, dk, dv, dv))
+    gam = binding.gamma_schedule(H).to(dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), None)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        binding.retention_backward(q, k, v, gam, do, want_dstate_in=False, grads=grads)
+    times = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.retention_backward(q, k, v, gam, do, want_dstate_in=False, grads=grads)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    return times
+
+
 def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
     """fp64 oracle (chunkwise form, same chunk) on the full workload, repeated for >= min_seconds."""
     import oracle
@@ -532,6 +579,24 @@ def run_ours(args):
             "config": {"workload": "mid retention chunkwise fwd + GroupNorm over each head (fused epilogue)",
                        "out_layout": "[B, N, H, dv]"},
             "gpu_launches": nf}
+        # gradients of the mid workload (CUDA-core fp32 kernel, one launch)
+        bt = statistics.median(time_backward(w, 10, dev, flush)) / 1e3
+        props = torch.cuda.get_device_properties(dev)
+        max_mhz = clk.summary().get("sm_max_mhz") or 2032
+        fp32_peak = props.multi_processor_count * 128 * 2 * max_mhz * 1e6 / 1e12
+        bflops = backward_flops(w, backward_chunk(w["dk"], w["dv"]))
+        extra["mid_backward"] = {
+            "tokens_per_s": round(w["B"] * w["N"] / bt, 1), "ms_per_call": round(bt * 1e3, 5),
+            "config": {"workload": "mid retention gradients (dq, dk, dv), no states", "B": w["B"], "H": w["H"],
+                       "N": w["N"], "dk": w["dk"], "dv": w["dv"],
+                       "internal_chunk": backward_chunk(w["dk"], w["dv"]),
+                       "l2": "flushed before each call (512 MiB write, then 512 MiB read)"},
+            "roofline": {"bound": "alu", "achieved": round(bflops / bt / 1e12, 2),
+                         "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
+                         "peak_kind": "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock",
+                         "frac": round(bflops / bt / 1e12 / fp32_peak, 4), "traffic": None,
+                         "hbm_frac": round(backward_bytes(w) / bt / 1e9 / hbm, 4)},
+            "gpu_launches": 1}
         for wl in (LONG, B7):
             t, n, _ = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
             a_s = statistics.median(t) / 1e3
@@ -614,6 +679,10 @@ def run_only(args):
         print(json.dumps({"only": "decode", "ms_per_step": statistics.median(t)}))
         return
     flush = L2Flush(dev)
+    if args.only == "backward":
+        t = time_backward(MID, args.steps, dev, flush)
+        print(json.dumps({"only": "backward", "ms_per_call": statistics.median(t), "launches": args.steps}))
+        return
     if args.only in ("groupnorm", "rotate"):
         fn, wl = (time_groupnorm, GROUPNORM) if args.only == "groupnorm" else (time_rotate, ROTATE)
         t = fn(wl, args.steps, dev, flush)
@@ -632,7 +701,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate"], default=None)
+    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate", "backward"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -264,6 +264,44 @@ int retention_step_f32(const float *q, const float *k, const float *v, float *st
                        int B, int H, int dk, int dv, void *stream);
 
 /*
+ * retention_backward -- gradients of the forward (any of its forms: they
+ * compute one function), for training.  "3. The Chunkwise Recurrent
+ * Representation ..." gives the chunkwise form as the way to train on long
+ * sequences but prints no gradient; these are the partial derivatives of the
+ * forward started from state_in (S0),
+ *
+ *   out_n = s [ sum_{m<=n} g^(n-m) (q_n . k_m) v_m + g^(n+1) q_n S0 ],
+ *   S_N   = g^N S0 + sum_m g^(N-1-m) k_m^T v_m          (s = 1/sqrt(dk), g = gamma[h]),
+ *
+ * for the loss <dout, out> + <dstate, S_N>:
+ *
+ *   dq_n  = s [ sum_{m<=n} g^(n-m) (dout_n . v_m) k_m + g^(n+1) S0 dout_n ]
+ *   dk_m  = s sum_{n>=m} g^(n-m) (dout_n . v_m) q_n + g^(N-1-m) dstate v_m
+ *   dv_m  = s sum_{n>=m} g^(n-m) (q_n . k_m) dout_n + g^(N-1-m) k_m dstate
+ *   dS0   = s sum_n g^(n+1) q_n^T dout_n + g^N dstate
+ *
+ * q, k, dq, dk: bf16 [B][H][N][dk]; v, dout, dv: bf16 [B][H][N][dv]; gamma:
+ * float32 [H]; state_in, dstate, dstate_in: float32 [B][H][dk][dv]; all
+ * row-major device memory, 16-byte aligned, owned by the caller.  state_in
+ * and dstate may be NULL (zero); dstate_in may be NULL (not written).  The
+ * gradients are written, not accumulated.  Outputs must not overlap inputs or
+ * one another (dstate_in equal to dstate or state_in returns
+ * RET_ERR_INVALID).  When N == 0, dstate_in receives a copy of dstate (zero if
+ * NULL).  Arithmetic is float32 on the CUDA cores, one launch, no workspace.
+ * Supported: dk, dv multiples of 4, at most 512; other widths return
+ * RET_ERR_UNSUPPORTED.
+ * retention_backward_f32 is the same with float32 q/k/v/dout/dq/dk/dv.
+ */
+int retention_backward(const void *q, const void *k, const void *v, const float *gamma,
+                       const float *state_in, const void *dout, const float *dstate,
+                       void *dq, void *dk_out, void *dv_out, float *dstate_in,
+                       int B, int H, int N, int dk, int dv, void *stream);
+int retention_backward_f32(const float *q, const float *k, const float *v, const float *gamma,
+                           const float *state_in, const float *dout, const float *dstate,
+                           float *dq, float *dk_out, float *dv_out, float *dstate_in,
+                           int B, int H, int N, int dk, int dv, void *stream);
+
+/*
  * retention_gamma_schedule -- host function: gamma_out[h] = 1 - 2^(-5-h),
  * h = 0..H-1, rounded to float32 ("3. Multi-Scale Retention (MSR)",
  * 0-based heads).  gamma_out is HOST memory of H floats.

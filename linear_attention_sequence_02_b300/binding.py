@@ -46,6 +46,8 @@ _SIGNATURES = {
     "retention_parallel_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "retention_groupnorm": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _vp],
     "retention_rotate": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+    "retention_backward": [_vp] * 11 + [_i] * 5 + [_vp],
+    "retention_backward_f32": [_vp] * 11 + [_i] * 5 + [_vp],
     "retention_step": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_step_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_gamma_schedule": [_i, _fp],
@@ -299,6 +301,48 @@ def retention_rotate(x, theta, n0: int = 0, out=None, stream=None):
     _check("retention_rotate", lib().retention_rotate(_p(x), _p(theta), _p(out), B, H, N, d, int(n0),
                                                       _stream(stream)))
     return out
+
+
+def _backward(fn, dtype, q, k, v, gamma, dout, dstate, state_in, want_dstate_in, grads, stream):
+    B, H, N, dk, dv = _seq_dims(q, v)
+    _need(q, "q", dtype, (B, H, N, dk))
+    _need(k, "k", dtype, (B, H, N, dk))
+    _need(v, "v", dtype, (B, H, N, dv))
+    _need(dout, "dout", dtype, (B, H, N, dv))
+    _need(gamma, "gamma", torch.float32, (H,))
+    for t, name in ((state_in, "state_in"), (dstate, "dstate")):
+        if t is not None:
+            _need(t, name, torch.float32, (B, H, dk, dv))
+    dq, dk_, dv_, ds0 = grads if grads is not None else (None, None, None, None)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk_ = torch.empty_like(k) if dk_ is None else dk_
+    dv_ = torch.empty_like(v) if dv_ is None else dv_
+    if ds0 is None and want_dstate_in:
+        ds0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _need(dq, "dq", dtype, (B, H, N, dk))
+    _need(dk_, "dk", dtype, (B, H, N, dk))
+    _need(dv_, "dv", dtype, (B, H, N, dv))
+    if ds0 is not None:
+        _need(ds0, "dstate_in", torch.float32, (B, H, dk, dv))
+    _check(fn, getattr(lib(), fn)(_p(q), _p(k), _p(v), _p(gamma), _p(state_in), _p(dout), _p(dstate),
+                                  _p(dq), _p(dk_), _p(dv_), _p(ds0), B, H, N, dk, dv, _stream(stream)))
+    return dq, dk_, dv_, ds0
+
+
+def retention_backward(q, k, v, gamma, dout, dstate=None, state_in=None, want_dstate_in: bool = True,
+                       grads=None, stream=None):
+    """Gradients of <dout, out> + <dstate, final state> for the bf16 forward
+    started from state_in (zero if None); returns (dq, dk, dv, dstate_in),
+    dstate_in None when not wanted.  `grads` may pass the four output tensors."""
+    return _backward("retention_backward", torch.bfloat16, q, k, v, gamma, dout, dstate, state_in,
+                     want_dstate_in, grads, stream)
+
+
+def retention_backward_f32(q, k, v, gamma, dout, dstate=None, state_in=None, want_dstate_in: bool = True,
+                           grads=None, stream=None):
+    """retention_backward with fp32 q, k, v, dout and gradients."""
+    return _backward("retention_backward_f32", torch.float32, q, k, v, gamma, dout, dstate, state_in,
+                     want_dstate_in, grads, stream)
 
 
 def _step(fn, dtype, q, k, v, state, out, stream):

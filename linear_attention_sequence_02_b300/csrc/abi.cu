@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points declared in include/retention.h:
 // argument validation (host only, before anything is enqueued), planning and
-// dispatch to the kernels in simt.cu and chunk_tc.cu.
+// dispatch to the kernels in simt.cu, chunk_tc.cu, backward.cu, rotate.cu and
+// groupnorm.cu.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -96,6 +97,35 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
     if (e == cudaSuccess) e = e2;
   }
   return from_cuda(e);
+}
+
+// Gradients of the forward, bf16 or fp32 tensors (see retention_backward).
+int backward_call(bool bf16, const void* q, const void* k, const void* v, const float* gamma,
+                  const float* state_in, const void* dout, const float* dstate, void* dq, void* dk_out,
+                  void* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv, void* stream) {
+  int st = check_sequence(q, k, v, gamma, dout, nullptr, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  if (N > 0) {
+    if (!dq || !dk_out || !dv_out) return RET_ERR_INVALID;
+    if (!aligned(dq, 16) || !aligned(dk_out, 16) || !aligned(dv_out, 16)) return RET_ERR_INVALID;
+  }
+  if ((state_in && !aligned(state_in, 16)) || (dstate && !aligned(dstate, 16)) ||
+      (dstate_in && !aligned(dstate_in, 16)))
+    return RET_ERR_INVALID;
+  if (dstate_in && (dstate_in == dstate || dstate_in == state_in)) return RET_ERR_INVALID;
+  if (dk % 4 != 0 || dv % 4 != 0 || dk > 512 || dv > 512 ||
+      ret::backward_smem_bytes(dk, dv) > (size_t)ret::kMaxSmemPerBlock)
+    return RET_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    // the gradient reaches the starting state unchanged through no tokens
+    if (!dstate_in) return RET_OK;
+    if (!dstate) return zero_state(dstate_in, B, H, dk, dv, s);
+    return from_cuda(cudaMemcpyAsync(dstate_in, dstate, sizeof(float) * (size_t)B * H * dk * dv,
+                                     cudaMemcpyDeviceToDevice, s));
+  }
+  return from_cuda(ret::launch_backward(bf16, q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out,
+                                        dstate_in, B, H, N, dk, dv, s));
 }
 
 }  // namespace
@@ -256,6 +286,21 @@ int retention_parallel_f32(const float* q, const float* k, const float* v, const
   if (B * H > 65535) return RET_ERR_UNSUPPORTED;
   return from_cuda(ret::launch_parallel_f32(q, k, v, gamma, out, B, H, N, dk, dv,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+int retention_backward(const void* q, const void* k, const void* v, const float* gamma,
+                       const float* state_in, const void* dout, const float* dstate, void* dq, void* dk_out,
+                       void* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv, void* stream) {
+  return backward_call(true, q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out, dstate_in, B, H, N, dk,
+                       dv, stream);
+}
+
+int retention_backward_f32(const float* q, const float* k, const float* v, const float* gamma,
+                           const float* state_in, const float* dout, const float* dstate, float* dq,
+                           float* dk_out, float* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv,
+                           void* stream) {
+  return backward_call(false, q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out, dstate_in, B, H, N, dk,
+                       dv, stream);
 }
 
 int retention_step(const void* q, const void* k, const void* v, float* state, void* out, int B,

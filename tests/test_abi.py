@@ -129,3 +129,27 @@ def test_chunkwise_groupnorm_validation(lib):
     assert fn(P, P, P, P, ctypes.c_void_p(0x1008), None, 1e-6, P, None, 1, 1, 8, 128, 128, 64, None) == \
         binding.RET_ERR_INVALID
     assert fn(None, P, P, P, None, None, 1e-6, P, None, 1, 1, 8, 128, 128, 64, None) == binding.RET_ERR_INVALID
+
+
+def test_backward_validation(lib):
+    """Host checks of the gradient call: required pointers present and
+    aligned, the starting-state gradient not written over dstate or state_in,
+    widths above 512 or not a multiple of 4 refused."""
+    P2, P3 = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    for fn in (lib.retention_backward, lib.retention_backward_f32):
+        # (q, k, v, gamma, state_in, dout, dstate, dq, dk, dv, dstate_in, B, H, N, dk, dv, stream)
+        assert fn(None, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, None, None, P, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, P, None, None, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, P, None, P, P, P_ODD, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, P_ODD, P, None, P, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, P, P2, P, P, P, P2, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, P3, P, P2, P, P, P, P3, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 0, 8, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, -1, 64, 64, None) == binding.RET_ERR_INVALID
+        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 64, 640, None) == binding.RET_ERR_UNSUPPORTED
+        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 1024, 64, None) == binding.RET_ERR_UNSUPPORTED
+        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 66, 64, None) == binding.RET_ERR_UNSUPPORTED
+        # nothing to do: no tokens and no starting-state gradient wanted
+        assert fn(None, None, None, None, None, None, None, None, None, None, None, 1, 1, 0, 64, 64, None) == \
+            binding.RET_OK

@@ -1,0 +1,100 @@
+"""GPU parity of retention_backward (gradients of the forward with respect to
+q, k, v and the starting state) against the fp64 oracle's derivatives.
+
+Cases cover several internal chunks with a ragged last one, widths that are
+not multiples of the 32-column slab, d_k != d_v, the widest rows (d_k 256,
+d_v 512, where the kernel uses shorter chunks), a starting state and a
+final-state gradient (each present or absent), decays 0, 0.5, 0.9 and 1, the
+fp32 twin, an empty sequence, and the mid workload (4 x 8 heads, N 2048,
+d 128), compared on a subset of heads: heads are independent, so the oracle
+on those heads alone gives their exact gradients.
+"""
+import pytest
+import torch
+
+from _compare import TOL_BF16, TOL_F32, assert_close
+from linear_attention_sequence_02_b300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(B, H, N, dk, dv, seed, dtype, states):
+    q, k, v = inputs.qkv(B, H, N, dk, dv, seed, dtype)
+    dout = inputs.normal((B, H, N, dv), 1000 + seed, dtype)
+    s0 = inputs.normal((B, H, dk, dv), 2000 + seed, torch.float32) if states else None
+    ds = inputs.normal((B, H, dk, dv), 3000 + seed, torch.float32) if states else None
+    return q, k, v, dout, s0, ds
+
+
+def _gpu(x):
+    return None if x is None else x.to(DEV)
+
+
+def _check(orc, q, k, v, g, dout, s0, ds, tol, f32=False, what=""):
+    ref = orc.backward(q, k, v, g.double(), dout, ds, s0)
+    fn = binding.retention_backward_f32 if f32 else binding.retention_backward
+    got = fn(_gpu(q), _gpu(k), _gpu(v), _gpu(g), _gpu(dout), _gpu(ds), _gpu(s0))
+    torch.cuda.synchronize()
+    for name, a, b in zip(("dq", "dk", "dv", "dstate_in"), got, ref):
+        assert_close(a.cpu(), b, tol, f"{what} {name}")
+
+
+@pytest.mark.parametrize("B,H,N,dk,dv,states", [
+    (1, 2, 300, 128, 128, False),   # five internal chunks, ragged last one
+    (1, 2, 300, 128, 128, True),
+    (2, 3, 77, 64, 32, True),
+    (1, 2, 200, 32, 96, True),      # d_k != d_v
+    (1, 2, 130, 40, 24, True),      # slabs of 8 columns at the edge
+    (1, 1, 100, 256, 512, True),    # widest rows: chunks of 32
+    (1, 2, 1, 128, 128, True),      # one token
+])
+def test_backward_matches_oracle(orc, B, H, N, dk, dv, states):
+    q, k, v, dout, s0, ds = _case(B, H, N, dk, dv, 5, torch.bfloat16, states)
+    g = binding.gamma_schedule(H)
+    _check(orc, q, k, v, g, dout, s0, ds, TOL_BF16, what=f"bf16 {B}x{H}x{N} {dk}/{dv}")
+
+
+def test_backward_any_decay_and_one_state(orc):
+    gam = [0.0, 0.5, 0.9, 1.0]
+    H, N, dk, dv = len(gam), 170, 64, 64
+    g = torch.tensor(gam, dtype=torch.float32)
+    q, k, v, dout, s0, ds = _case(1, H, N, dk, dv, 6, torch.bfloat16, True)
+    _check(orc, q, k, v, g, dout, s0, None, TOL_BF16, what="any decay, starting state only")
+    _check(orc, q, k, v, g, dout, None, ds, TOL_BF16, what="any decay, final-state gradient only")
+
+
+@pytest.mark.parametrize("B,H,N,dk,dv", [(1, 2, 150, 64, 64), (1, 3, 65, 32, 48)])
+def test_backward_f32_matches_oracle(orc, B, H, N, dk, dv):
+    q, k, v, dout, s0, ds = _case(B, H, N, dk, dv, 7, torch.float32, True)
+    g = binding.gamma_schedule(H)
+    _check(orc, q, k, v, g, dout, s0, ds, TOL_F32, f32=True, what="fp32")
+
+
+def test_backward_empty_sequence():
+    B, H, dk, dv = 1, 2, 64, 32
+    z = torch.zeros(B, H, 0, dk, dtype=torch.bfloat16, device=DEV)
+    zv = torch.zeros(B, H, 0, dv, dtype=torch.bfloat16, device=DEV)
+    ds = inputs.normal((B, H, dk, dv), 9, torch.float32).to(DEV)
+    g = binding.gamma_schedule(H).to(DEV)
+    _, _, _, ds0 = binding.retention_backward(z, z, zv, g, zv, ds)
+    torch.cuda.synchronize()
+    assert torch.equal(ds0, ds)
+    _, _, _, ds0 = binding.retention_backward(z, z, zv, g, zv)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(ds0) == 0
+
+
+def test_backward_mid_workload_sampled_heads(orc):
+    """Full mid workload on the GPU; the oracle's gradients for heads 0 and 7
+    of every batch row (the fastest and slowest decay)."""
+    B, H, N, dk, dv = 4, 8, 2048, 128, 128
+    q, k, v, dout, s0, ds = _case(B, H, N, dk, dv, 8, torch.bfloat16, True)
+    g = binding.gamma_schedule(H)
+    got = binding.retention_backward(_gpu(q), _gpu(k), _gpu(v), _gpu(g), _gpu(dout), _gpu(ds), _gpu(s0))
+    torch.cuda.synchronize()
+    heads = [0, H - 1]
+    ref = orc.backward(q[:, heads], k[:, heads], v[:, heads], g[heads].double(), dout[:, heads],
+                       ds[:, heads], s0[:, heads])
+    for name, a, b in zip(("dq", "dk", "dv", "dstate_in"), got, ref):
+        assert_close(a[:, heads].cpu(), b, TOL_BF16, f"mid workload {name}")
