@@ -428,9 +428,8 @@ def time_rotate(w, reps, dev, flush, seed=0):
 
 
 def backward_chunk(dk: int, dv: int) -> int:
-    """The chunk length the gradient kernel uses inside: 64 while both widths
-    are at most 256, else 32 (so its shared-memory tiles fit one CTA)."""
-    return 32 if max(dk, dv) > 256 else 64
+    """The chunk length the gradient kernel uses inside (32 for every width)."""
+    return 32
 
 
 def backward_flops(w, C: int) -> int:

@@ -32,16 +32,19 @@
 //   dv     backward   k     q     dout  G[c][t]  (t over dv, c over dk)
 // One CTA per (b h, role, 32-column slab) walks the chunks with its slab in
 // shared memory; one launch makes every gradient.  The chunk length inside
-// the kernel is its own choice (the gradients do not depend on it): 64, or 32
-// when a row is wider than 256 (so the tiles fit one CTA).
+// the kernel is its own choice (the gradients do not depend on it): 32, which
+// costs less arithmetic per token than 64 (the scores, recomputed by every
+// slab, grow with the chunk) and keeps the tiles at 60 KB for rows of 128, so
+// three CTAs share an SM.
 //
 // Each chunk is four phases separated by barriers: load (a, b rows row-major,
-// the w slab transposed), scores (a 4x4 (2x2 at chunk 32) register tile per
-// thread over float4 loads), gradient rows (2x4 / 1x4 per thread), state
-// update (4x4 per thread per 128 columns).  Rows a thread owns are strided
-// (16 or 8 apart) so that the eight lanes of a quarter warp read distinct
-// bank groups.  The phase bodies are __host__ __device__ functions of the
-// thread index, so the same code can be stepped thread by thread on a CPU.
+// the w slab transposed; each thread issues all its global loads before it
+// stores any), scores (a 2x2 register tile per thread over float4 loads),
+// gradient rows (1x4 per thread), state update (4x4 per thread per 128
+// columns).  Rows a thread owns are strided (16 or 8 apart) so that the eight
+// lanes of a quarter warp read distinct bank groups.  The phase bodies are
+// __host__ __device__ functions of the thread index, so the same code can be
+// stepped thread by thread on a CPU.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -54,6 +57,8 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdSlab = 32;  // gradient columns per CTA
+constexpr int kBwdChunk = 32; // chunk length inside the kernel
+constexpr int kBwdLoadBatch = 4;  // loads a thread has in flight in the load phase
 
 struct BwdArgs {
   const void* q;
@@ -184,15 +189,27 @@ __host__ __device__ inline void bwd_load(const BwdArgs& p, const BwdRole& r, con
   const T* Bm = r.role == 0 ? V : (r.role == 1 ? DO : Q);
   const T* W = r.role == 0 ? K : (r.role == 1 ? Q : DO);
   const int w4 = r.wa / 4;
-  for (int e = tid; e < C * w4; e += kBwdThreads) {
-    const int j = e / w4, c = 4 * (e % w4);
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-    if (j < L) {
-      a = ld4(A + (size_t)(s0 + j) * r.wa + c);
-      b = ld4(Bm + (size_t)(s0 + j) * r.wa + c);
+  for (int e0 = tid; e0 < C * w4; e0 += kBwdLoadBatch * kBwdThreads) {
+    float4 a[kBwdLoadBatch], b[kBwdLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kBwdLoadBatch; ++u) {
+      const int e = e0 + u * kBwdThreads;
+      const int j = e / w4, c = 4 * (e % w4);
+      a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < C * w4 && j < L) {
+        a[u] = ld4(A + (size_t)(s0 + j) * r.wa + c);
+        b[u] = ld4(Bm + (size_t)(s0 + j) * r.wa + c);
+      }
     }
-    *reinterpret_cast<float4*>(s.As + (size_t)j * s.lda + c) = a;
-    *reinterpret_cast<float4*>(s.Bs + (size_t)j * s.lda + c) = b;
+#pragma unroll
+    for (int u = 0; u < kBwdLoadBatch; ++u) {
+      const int e = e0 + u * kBwdThreads;
+      const int j = e / w4, c = 4 * (e % w4);
+      if (e < C * w4) {
+        *reinterpret_cast<float4*>(s.As + (size_t)j * s.lda + c) = a[u];
+        *reinterpret_cast<float4*>(s.Bs + (size_t)j * s.lda + c) = b[u];
+      }
+    }
   }
   for (int e = tid; e < C * (kBwdSlab / 4); e += kBwdThreads) {
     const int l = e / (kBwdSlab / 4), t = 4 * (e % (kBwdSlab / 4));
@@ -212,7 +229,9 @@ __host__ __device__ inline void bwd_scores(const BwdRole& r, const BwdSmem<C>& s
   constexpr int M = C / 16;
   const int tj = tid / 16, tl = tid % 16;
   float acc[M][M];
+#pragma unroll
   for (int x = 0; x < M; ++x)
+#pragma unroll
     for (int y = 0; y < M; ++y) acc[x][y] = 0.f;
   for (int c = 0; c < r.wa; c += 4) {
     float4 a[M], b[M];
@@ -244,7 +263,9 @@ __host__ __device__ inline void bwd_rows(const BwdArgs& p, const BwdRole& r, con
   const int rj = tid / 8, rt = tid % 8;
   const int Lr = (L + 3) & ~3;
   float inner[MY][4], cross[MY][4];
+#pragma unroll
   for (int y = 0; y < MY; ++y)
+#pragma unroll
     for (int x = 0; x < 4; ++x) inner[y][x] = cross[y][x] = 0.f;
   for (int l = 0; l < Lr; l += 4) {
     float4 pj[MY], wt[4];
@@ -293,6 +314,7 @@ __host__ __device__ inline void bwd_update(const BwdRole& r, const BwdSmem<C>& s
   const float gL = s.pw[L];
   for (int c = 4 * ug; c < r.wa; c += 4 * (kBwdThreads / 8)) {
     float4 u[4];
+#pragma unroll
     for (int x = 0; x < 4; ++x) u[x] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int l = 0; l < Lr; l += 4) {
       float cf[4];
@@ -340,7 +362,7 @@ __host__ __device__ inline void bwd_final(const BwdArgs& p, const BwdRole& r, co
 }
 
 template <int C, typename T>
-__global__ void __launch_bounds__(kBwdThreads) backward_kernel(BwdArgs p) {
+__global__ void __launch_bounds__(kBwdThreads, 3) backward_kernel(BwdArgs p) {
   extern __shared__ float4 sm4[];
   const BwdRole r = bwd_role(p, blockIdx.x, blockIdx.y);
   const BwdSmem<C> s(reinterpret_cast<float*>(sm4), p.wmax);
@@ -375,11 +397,10 @@ cudaError_t launch_bwd(const BwdArgs& a, int BH, cudaStream_t s) {
 
 }  // namespace
 
-int backward_chunk(int dk, int dv) { return (dk > 256 || dv > 256) ? 32 : 64; }
+int backward_chunk(int, int) { return kBwdChunk; }
 
 size_t backward_smem_bytes(int dk, int dv) {
-  const int wmax = dk > dv ? dk : dv;
-  return sizeof(float) * (backward_chunk(dk, dv) == 64 ? BwdSmem<64>::floats(wmax) : BwdSmem<32>::floats(wmax));
+  return sizeof(float) * BwdSmem<kBwdChunk>::floats(dk > dv ? dk : dv);
 }
 
 cudaError_t launch_backward(bool bf16, const void* q, const void* k, const void* v, const float* gamma,
@@ -405,9 +426,7 @@ cudaError_t launch_backward(bool bf16, const void* q, const void* k, const void*
   a.slabs_v = (dv + kBwdSlab - 1) / kBwdSlab;
   a.wmax = dk > dv ? dk : dv;
   const int BH = B * H;
-  if (backward_chunk(dk, dv) == 64)
-    return bf16 ? launch_bwd<64, __nv_bfloat16>(a, BH, s) : launch_bwd<64, float>(a, BH, s);
-  return bf16 ? launch_bwd<32, __nv_bfloat16>(a, BH, s) : launch_bwd<32, float>(a, BH, s);
+  return bf16 ? launch_bwd<kBwdChunk, __nv_bfloat16>(a, BH, s) : launch_bwd<kBwdChunk, float>(a, BH, s);
 }
 
 }  // namespace ret

@@ -3,11 +3,11 @@ q, k, v and the starting state) against the fp64 oracle's derivatives.
 
 Cases cover several internal chunks with a ragged last one, widths that are
 not multiples of the 32-column slab, d_k != d_v, the widest rows (d_k 256,
-d_v 512, where the kernel uses shorter chunks), a starting state and a
-final-state gradient (each present or absent), decays 0, 0.5, 0.9 and 1, the
-fp32 twin, an empty sequence, and the mid workload (4 x 8 heads, N 2048,
-d 128), compared on a subset of heads: heads are independent, so the oracle
-on those heads alone gives their exact gradients.
+d_v 512), a starting state and a final-state gradient (each present or
+absent), decays 0, 0.5, 0.9 and 1, the fp32 twin, an empty sequence, and the
+mid workload (4 x 8 heads, N 2048, d 128), compared on a subset of heads:
+heads are independent, so the oracle on those heads alone gives their exact
+gradients.
 """
 import pytest
 import torch
@@ -41,12 +41,12 @@ def _check(orc, q, k, v, g, dout, s0, ds, tol, f32=False, what=""):
 
 
 @pytest.mark.parametrize("B,H,N,dk,dv,states", [
-    (1, 2, 300, 128, 128, False),   # five internal chunks, ragged last one
+    (1, 2, 300, 128, 128, False),   # ten internal chunks, ragged last one
     (1, 2, 300, 128, 128, True),
     (2, 3, 77, 64, 32, True),
     (1, 2, 200, 32, 96, True),      # d_k != d_v
     (1, 2, 130, 40, 24, True),      # slabs of 8 columns at the edge
-    (1, 1, 100, 256, 512, True),    # widest rows: chunks of 32
+    (1, 1, 100, 256, 512, True),    # widest rows
     (1, 2, 1, 128, 128, True),      # one token
 ])
 def test_backward_matches_oracle(orc, B, H, N, dk, dv, states):
