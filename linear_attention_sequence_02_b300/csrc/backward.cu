@@ -224,8 +224,10 @@ __host__ __device__ inline void bwd_load(const BwdArgs& p, const BwdRole& r, con
 
 // P[j][l] = g^|j-l| a_j . b_l on the causal side (l <= j forward, l >= j
 // backward) inside the chunk, else 0.  Thread: rows j = tj + 16x, l = tl + 16y.
-template <int C>
-__host__ __device__ inline void bwd_scores(const BwdRole& r, const BwdSmem<C>& s, int L, int tid) {
+// Since |tj - tl| < 16, the pairs with y > x (forward) or y < x (backward)
+// are always on the masked side: they are written as 0 without a product.
+template <int C, bool FWD>
+__host__ __device__ inline void bwd_scores(const BwdSmem<C>& s, int wa, int L, int tid) {
   constexpr int M = C / 16;
   const int tj = tid / 16, tl = tid % 16;
   float acc[M][M];
@@ -233,7 +235,7 @@ __host__ __device__ inline void bwd_scores(const BwdRole& r, const BwdSmem<C>& s
   for (int x = 0; x < M; ++x)
 #pragma unroll
     for (int y = 0; y < M; ++y) acc[x][y] = 0.f;
-  for (int c = 0; c < r.wa; c += 4) {
+  for (int c = 0; c < wa; c += 4) {
     float4 a[M], b[M];
 #pragma unroll
     for (int x = 0; x < M; ++x) a[x] = ld4(s.As + (size_t)(tj + 16 * x) * s.lda + c);
@@ -242,16 +244,25 @@ __host__ __device__ inline void bwd_scores(const BwdRole& r, const BwdSmem<C>& s
 #pragma unroll
     for (int x = 0; x < M; ++x)
 #pragma unroll
-      for (int y = 0; y < M; ++y) acc[x][y] = dot4(a[x], b[y], acc[x][y]);
+      for (int y = 0; y < M; ++y)
+        if (FWD ? y <= x : y >= x) acc[x][y] = dot4(a[x], b[y], acc[x][y]);
   }
 #pragma unroll
   for (int x = 0; x < M; ++x)
 #pragma unroll
     for (int y = 0; y < M; ++y) {
       const int j = tj + 16 * x, l = tl + 16 * y;
-      const bool keep = j < L && l < L && (r.fwd ? l <= j : l >= j);
-      s.P[j * s.ldp + l] = keep ? s.pw[r.fwd ? j - l : l - j] * acc[x][y] : 0.f;
+      const bool keep = j < L && l < L && (FWD ? l <= j : l >= j);
+      s.P[j * s.ldp + l] = keep ? s.pw[FWD ? j - l : l - j] * acc[x][y] : 0.f;
     }
+}
+
+template <int C>
+__host__ __device__ inline void bwd_scores(const BwdRole& r, const BwdSmem<C>& s, int L, int tid) {
+  if (r.fwd)
+    bwd_scores<C, true>(s, r.wa, L, tid);
+  else
+    bwd_scores<C, false>(s, r.wa, L, tid);
 }
 
 // Gradient rows: in-chunk sum over P and the w slab, plus the cross term of a
@@ -262,12 +273,16 @@ __host__ __device__ inline void bwd_rows(const BwdArgs& p, const BwdRole& r, con
   constexpr int MY = C / 32;
   const int rj = tid / 8, rt = tid % 8;
   const int Lr = (L + 3) & ~3;
+  // P is zero off the causal side, so the inner sum runs over the 4-column
+  // groups that hold l <= j (forward) or l >= j (backward) for this thread's j
+  const int l_begin = r.fwd ? 0 : (rj & ~3);
+  const int l_end = r.fwd ? imin(Lr, ((rj + 32 * (MY - 1)) | 3) + 1) : Lr;
   float inner[MY][4], cross[MY][4];
 #pragma unroll
   for (int y = 0; y < MY; ++y)
 #pragma unroll
     for (int x = 0; x < 4; ++x) inner[y][x] = cross[y][x] = 0.f;
-  for (int l = 0; l < Lr; l += 4) {
+  for (int l = l_begin; l < l_end; l += 4) {
     float4 pj[MY], wt[4];
 #pragma unroll
     for (int y = 0; y < MY; ++y) pj[y] = ld4(s.P + (rj + 32 * y) * s.ldp + l);
