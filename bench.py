@@ -24,7 +24,8 @@ Also reported on the same line:
 
 `--impl reference` times the fp64 CPU oracle alone on the same workload and
 metric (the full mid workload per step) and prints its own line.
-`--only {mid,long,7b,decode,groupnorm,rotate,backward}` runs one workload alone and prints its timing
+`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b}`
+runs one workload alone and prints its timing
 (used to give ncu a small, single-workload command).
 Under torchrun each rank runs its own replica (independent batches, no
 collective on the data path); value = all ranks' tokens / max rank time.
@@ -678,9 +679,11 @@ def run_only(args):
         print(json.dumps({"only": "decode", "ms_per_step": statistics.median(t)}))
         return
     flush = L2Flush(dev)
-    if args.only == "backward":
-        t = time_backward(MID, args.steps, dev, flush)
-        print(json.dumps({"only": "backward", "ms_per_call": statistics.median(t), "launches": args.steps}))
+    if args.only in ("backward", "backward_long", "backward_7b"):
+        wl = {"backward": MID, "backward_long": LONG, "backward_7b": B7}[args.only]
+        t = time_backward(wl, args.steps, dev, flush)
+        print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps,
+                          "tokens_per_s": round(wl["B"] * wl["N"] / (statistics.median(t) / 1e3), 1)}))
         return
     if args.only in ("groupnorm", "rotate"):
         fn, wl = (time_groupnorm, GROUPNORM) if args.only == "groupnorm" else (time_rotate, ROTATE)
@@ -700,7 +703,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate", "backward"], default=None)
+    ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate", "backward", "backward_long",
+                                       "backward_7b"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
