@@ -228,6 +228,12 @@ def barrier(world):
         dist.barrier()
 
 
+def whole_job_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: the units all ranks
+    processed divided by the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     if world == 1:
         return x
@@ -507,13 +513,12 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        times, launches, how = time_chunkwise(w, args.steps, args.warmup, dev, flush)
+        times, launches, how = time_chunkwise(w, args.steps, args.warmup, dev, flush, seed=rank)
     torch.cuda.synchronize(dev)
     barrier(world)
     total_ms = max_over_ranks(sum(times), world, dev)
     ms = total_ms / args.steps
-    tokens = w["B"] * w["N"] * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_rate(w["B"] * w["N"] * args.steps, world, total_ms / 1e3)
     avg_s = sum(times) / len(times) / 1e3
     achieved = chunk_bytes(w) / avg_s / 1e9
     traffic = recorded_traffic(w["name"])
@@ -524,9 +529,9 @@ def run_ours(args):
                 "tensor_flops_frac": round(chunk_flops(w) / avg_s / 1e12 / tflops, 4)}
 
     # ---- e2e through host buffers ----
-    e2e_ms, h2d, d2h = time_e2e(w, max(3, args.steps // 2), max(3, args.warmup), dev)
+    e2e_ms, h2d, d2h = time_e2e(w, max(3, args.steps // 2), max(3, args.warmup), dev, seed=rank)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    e2e = {"value": round(w["B"] * w["N"] * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+    e2e = {"value": round(whole_job_rate(w["B"] * w["N"], world, e2e_ms / 1e3), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     extra = {}
