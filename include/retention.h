@@ -22,6 +22,13 @@
  * query only; states hold unscaled k^T v sums, so a state produced by
  * retention_chunkwise can be advanced by retention_step.
  *
+ * Beyond the forward: retention_backward gives the gradients of the forward
+ * (the pages print none; they are the derivatives of the definition above),
+ * retention_rotate the position phase rotation of queries and keys
+ * ("2. Relative Position via Complex Exponential Phase Rotations"), and
+ * retention_groupnorm / retention_chunkwise_groupnorm the per-head GroupNorm
+ * of the multi-scale retention output ("1. The Parallel Representation ...").
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - All data pointers are DEVICE pointers on the current CUDA device, owned by
@@ -30,8 +37,9 @@
  *     q, k  [B][H][dk]          v, out  [B][H][dv]         (step calls)
  *     state, state_out  [B][H][dk][dv]  float32
  *     gamma  [H]  float32, each value in [0, 1]
- * - Element type: the base names take bfloat16 q, k, v, out; the *_f32 names
- *   take float32 q, k, v, out.  Accumulation is float32 everywhere.
+ * - Element type: the base names take bfloat16 q, k, v, out (and dout and
+ *   the gradients); the *_f32 names take float32.  Accumulation is float32
+ *   everywhere.
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *   asynchronous: they enqueue work on `stream` and never synchronise the
  *   device.  Inputs must stay valid until that work has run.
