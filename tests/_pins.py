@@ -420,6 +420,31 @@ def check_backward_gamma_one_is_library_autograd(o):
     _close(ds0, want_ds0, 1e-13, "dS0 at gamma = 1")
 
 
+def check_backward_scans_are_forward_retentions(o):
+    """Each gradient is a retention forward of permuted operands (decays > 0):
+    dq is the chunkwise form of (dout, v, k) from S0^T, times sqrt(dv)/sqrt(dk)
+    (that forward divides by the square root of its query width, dv); dv is
+    the time-reversed form of (k, q, dout) from dS/(s g); dk is the
+    time-reversed form of (v, dout, q) from dS^T/(s g), times s sqrt(dv); and
+    dS0 is s g times the final state of the reversed dv form (s = 1/sqrt(dk))."""
+    B, H, N, dk, dv = 1, 3, 37, 6, 10
+    g = np.array([0.9, 0.5, 0.99])
+    q, k = _rand((B, H, N, dk), 103), _rand((B, H, N, dk), 104)
+    v, dout = _rand((B, H, N, dv), 105), _rand((B, H, N, dv), 106)
+    S0, dS = _rand((B, H, dk, dv), 107), _rand((B, H, dk, dv), 108)
+    dq, dk_, dv_, ds0 = o.backward(q, k, v, g, dout, dS, S0)
+    s = 1.0 / math.sqrt(dk)
+    gs = g[None, :, None, None]
+    T = lambda x: np.ascontiguousarray(x.transpose(0, 1, 3, 2))
+    rev = lambda x: np.ascontiguousarray(x[:, :, ::-1])
+    fq, _ = o.chunkwise(dout, v, k, g, 8, state_in=T(S0))
+    _close(dq, fq * math.sqrt(dv) / math.sqrt(dk), 1e-13, "dq as a forward")
+    fv, sv = o.chunkwise(rev(k), rev(q), rev(dout), g, 8, state_in=dS / (s * gs))
+    _close(dv_, rev(fv), 1e-13, "dv as a reversed forward")
+    _close(ds0, s * gs * sv, 1e-13, "dS0 as the reversed forward's state")
+    fk, _ = o.chunkwise(rev(v), rev(dout), rev(q), g, 8, state_in=T(dS) / (s * gs))
+    _close(dk_, rev(fk) * math.sqrt(dv) * s, 1e-13, "dk as a reversed forward")
+
 def check_backward_empty_sequence(o):
     """N = 0: no gradients of the sequence; the starting state's gradient is dS."""
     q = np.zeros((1, 2, 0, 4))
@@ -452,5 +477,6 @@ ALL_CHECKS = [
     check_backward_brute_force_tiny,
     check_backward_euler_identities,
     check_backward_gamma_one_is_library_autograd,
+    check_backward_scans_are_forward_retentions,
     check_backward_empty_sequence,
 ]
