@@ -211,13 +211,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(self.samples), "source": self.source}
 
 
-def dist_setup():
+def dist_setup(backend: str | None = None):
+    """Rendezvous of the replicas (N > 1).  The backend is `backend`, else the
+    BENCH_DIST_BACKEND variable, else nccl when CUDA is present and gloo
+    otherwise; max_over_ranks then keeps its tensor on the matching device."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        backend = backend or os.environ.get("BENCH_DIST_BACKEND") or (
+            "nccl" if torch.cuda.is_available() else "gloo")
         dist.init_process_group(backend)
     return world, rank, local
 
@@ -238,6 +242,8 @@ def max_over_ranks(x: float, world: int, device) -> float:
     if world == 1:
         return x
     import torch.distributed as dist
+    if dist.get_backend() == "gloo":
+        device = torch.device("cpu")  # gloo reduces host tensors
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())

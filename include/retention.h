@@ -221,7 +221,8 @@ int retention_chunkwise_ws(const void *q, const void *k, const void *v, const fl
  * never used.
  * Set-up: the first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) once; make that first call
- * before any stream capture.
+ * before any stream capture.  A lookup that fails returns RET_ERR_CUDA and is
+ * tried again by the next call on that device; a successful one is kept.
  * Concurrency: every call on a device shares the one array, so calls whose
  * work overlaps on the GPU (different streams, or different host threads
  * without ordering) race on it; order them on one stream or serialise them.
@@ -293,8 +294,9 @@ int retention_step_f32(const float *q, const float *k, const float *v, float *st
  * row-major device memory, 16-byte aligned, owned by the caller.  state_in
  * and dstate may be NULL (zero); dstate_in may be NULL (not written).  The
  * gradients are written, not accumulated.  Outputs must not overlap inputs or
- * one another (dstate_in equal to dstate or state_in returns
- * RET_ERR_INVALID).  When N == 0, dstate_in receives a copy of dstate (zero if
+ * one another: a gradient whose bytes overlap q, k, v, dout or another
+ * gradient, or dstate_in equal to dstate or state_in, returns
+ * RET_ERR_INVALID.  When N == 0, dstate_in receives a copy of dstate (zero if
  * NULL).  Arithmetic is float32 on the CUDA cores, one launch, no workspace.
  * Supported: dk, dv multiples of 4, at most 512; other widths return
  * RET_ERR_UNSUPPORTED.

@@ -42,6 +42,16 @@ int check_step(const void* q, const void* k, const void* v, const float* state, 
   return RET_OK;
 }
 
+// A byte range [p, p + bytes) of device memory.
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+bool overlap(const Span& a, const Span& b) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a.bytes > 0 && b.bytes > 0 && a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? RET_OK : RET_ERR_CUDA; }
 
 // Zero the state of an empty sequence (the sum over no tokens).
@@ -113,6 +123,19 @@ int backward_call(bool bf16, const void* q, const void* k, const void* v, const 
       (dstate_in && !aligned(dstate_in, 16)))
     return RET_ERR_INVALID;
   if (dstate_in && (dstate_in == dstate || dstate_in == state_in)) return RET_ERR_INVALID;
+  if (N > 0) {
+    // The kernels read q, k, v and dout while other CTAs already write the
+    // gradients, so no gradient may overlap an input or another gradient.
+    const size_t el = bf16 ? 2 : 4, rows = (size_t)B * H * N;
+    const Span in[4] = {{q, rows * dk * el}, {k, rows * dk * el}, {v, rows * dv * el}, {dout, rows * dv * el}};
+    const Span outs[3] = {{dq, rows * dk * el}, {dk_out, rows * dk * el}, {dv_out, rows * dv * el}};
+    for (int i = 0; i < 3; ++i) {
+      for (const Span& x : in)
+        if (overlap(outs[i], x)) return RET_ERR_INVALID;
+      for (int j = i + 1; j < 3; ++j)
+        if (overlap(outs[i], outs[j])) return RET_ERR_INVALID;
+    }
+  }
   if (dk % 4 != 0 || dv % 4 != 0 || dk > 512 || dv > 512 ||
       ret::backward_smem_bytes(dk, dv) > (size_t)ret::kMaxSmemPerBlock)
     return RET_ERR_UNSUPPORTED;

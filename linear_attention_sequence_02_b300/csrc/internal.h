@@ -56,15 +56,16 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             float* workspace, const ChunkNorm* norm, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 
-// ---- position phase rotation of queries and keys (rotate.cu) -------------------
-// Gradients of the forward (backward.cu); the chunk length the kernel uses
-// inside and its dynamic shared memory for these widths.
+// ---- gradients of the forward on the CUDA cores (backward.cu) ------------------
+// The chunk length the kernel uses inside and its dynamic shared memory for
+// these widths.
 int backward_chunk(int dk, int dv);
 size_t backward_smem_bytes(int dk, int dv);
 cudaError_t launch_backward(bool bf16, const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, const void* dout, const float* dstate, void* dq, void* dk_out,
                             void* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv, cudaStream_t s);
 
+// ---- position phase rotation of queries and keys (rotate.cu) -------------------
 bool rotate_supported(int N, int d, int n0);
 cudaError_t launch_rotate_bf16(const void* x, const float* theta, void* y, int B, int H, int N, int d,
                                int n0, cudaStream_t s);

@@ -24,22 +24,24 @@ constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_lock[kMaxDevices];
+void* g_scratch[kMaxDevices];  // written under g_lock[dev], only with a successful lookup
 
 // Device address of g_static_scratch on device `dev`, which must be current.
 // The host-side symbol is only a stand-in and is never handed to a kernel.
-// The lookup runs once per device, on the first call that uses it.
+// Only a successful lookup is kept: a failed one (for instance an error left
+// pending by an earlier call) is tried again on the device's next call.
 cudaError_t static_scratch(int dev, void** ptr) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_once[dev], [dev] {
+  std::lock_guard<std::mutex> hold(g_lock[dev]);
+  if (g_scratch[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_static_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
     g_scratch[dev] = p;
-  });
+  }
   *ptr = g_scratch[dev];
-  return g_scratch_err[dev];
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -26,8 +26,7 @@
  *         are divided by sqrt(d); the recurrent query is divided by sqrt(d)
  *         before it reads the post-update state.
  *
- * Readings taken where the pages are silent or garbled (each is listed in the
- * repository's design notes):
+ * Readings taken where the pages are silent or garbled:
  *   R1  the head index h in gamma_h is 0-based (the executable statement on
  *       [G] iterates range(num_heads)).
  *   R2  the factor d_k^(-1/2) multiplies q only; the state holds unscaled
@@ -39,6 +38,9 @@
  *   R5  the recurrent output reads the state after the update.
  *   R6  a last chunk shorter than C (N not a multiple of C) uses its own length
  *       L in gamma^L and in the in-chunk weights.
+ *   R7  the phase rotation turns pairs (2j, 2j+1) of the real dimensions as
+ *       one complex coordinate with frequency theta_j, and query and key alike
+ *       by the angle (n0 + n) theta_j (see oracle_rotate).
  *
  * Layout: q, k are [B][H][N][dk], v and out are [B][H][N][dv], state is
  * [B][H][dk][dv], gamma is [H]; all row-major, all double.  The loops over
@@ -285,7 +287,7 @@ void oracle_groupnorm(const double *r, const double *weight, const double *bias,
 /*
  * [G] "2. Relative Position via Complex Exponential Phase Rotations": the
  * query and key at position n are multiplied by the phase e^(i n theta), so
- * that their product depends on n - m only.  Reading R8 (design notes): pairs
+ * that their product depends on n - m only.  Reading R7 (above): pairs
  * (2j, 2j+1) of the d real dimensions are the real and imaginary parts of one
  * complex coordinate with frequency theta_j, and with the real dot product the
  * kernels use, query and key are both rotated by the angle (n0 + n) theta_j,

@@ -427,8 +427,8 @@ def check_backward_scans_are_forward_retentions(o):
     the time-reversed form of (k, q, dout) from dS/(s g); dk is the
     time-reversed form of (v, dout, q) from dS^T/(s g), times s sqrt(dv); and
     dS0 is s g times the final state of the reversed dv form (s = 1/sqrt(dk))."""
-    B, H, N, dk, dv = 1, 3, 37, 6, 10
-    g = np.array([0.9, 0.5, 0.99])
+    B, H, N, dk, dv = 1, 4, 37, 6, 10
+    g = np.array([0.9, 0.5, 0.99, 1.0])  # 1.0: no decay at all, the edge of the schedule
     q, k = _rand((B, H, N, dk), 103), _rand((B, H, N, dk), 104)
     v, dout = _rand((B, H, N, dv), 105), _rand((B, H, N, dv), 106)
     S0, dS = _rand((B, H, dk, dv), 107), _rand((B, H, dk, dv), 108)
@@ -444,6 +444,35 @@ def check_backward_scans_are_forward_retentions(o):
     _close(ds0, s * gs * sv, 1e-13, "dS0 as the reversed forward's state")
     fk, _ = o.chunkwise(rev(v), rev(dout), rev(q), g, 8, state_in=T(dS) / (s * gs))
     _close(dk_, rev(fk) * math.sqrt(dv) * s, 1e-13, "dk as a reversed forward")
+
+def check_backward_zero_decay_as_forwards(o):
+    """Decay 0, where the division by s g of the previous pin does not exist:
+    dq is still the forward of (dout, v, k) from S0^T; dv and dk are the
+    reversed forwards from a zero state, and the final-state gradient reaches
+    the last token alone (0^0 = 1, every other power of 0 vanishes):
+    dv_{N-1} += k_{N-1} dS, dk_{N-1} += v_{N-1} dS^T, and dS0 = 0 when N > 0.
+    A second head with decay 0.7 runs beside it in the same calls."""
+    B, H, N, dk, dv = 2, 2, 19, 4, 6
+    g = np.array([0.0, 0.7])
+    q, k = _rand((B, H, N, dk), 113), _rand((B, H, N, dk), 114)
+    v, dout = _rand((B, H, N, dv), 115), _rand((B, H, N, dv), 116)
+    S0, dS = _rand((B, H, dk, dv), 117), _rand((B, H, dk, dv), 118)
+    dq, dk_, dv_, ds0 = o.backward(q, k, v, g, dout, dS, S0)
+    s = 1.0 / math.sqrt(dk)
+    T = lambda x: np.ascontiguousarray(x.transpose(0, 1, 3, 2))
+    rev = lambda x: np.ascontiguousarray(x[:, :, ::-1])
+    fq, _ = o.chunkwise(dout, v, k, g, 5, state_in=T(S0))
+    _close(dq[:, :1], (fq * math.sqrt(dv) / math.sqrt(dk))[:, :1], 1e-13, "dq as a forward, decay 0")
+    fv, _ = o.chunkwise(rev(k), rev(q), rev(dout), g, 5)
+    want_dv = rev(fv)[:, :1].copy()
+    want_dv[:, 0, N - 1] += np.einsum("bi,bij->bj", k[:, 0, N - 1], dS[:, 0])
+    _close(dv_[:, :1], want_dv, 1e-13, "dv as a reversed forward plus the last token's dS term, decay 0")
+    fk, _ = o.chunkwise(rev(v), rev(dout), rev(q), g, 5)
+    want_dk = (rev(fk) * math.sqrt(dv) * s)[:, :1].copy()
+    want_dk[:, 0, N - 1] += np.einsum("bj,bij->bi", v[:, 0, N - 1], dS[:, 0])
+    _close(dk_[:, :1], want_dk, 1e-13, "dk as a reversed forward plus the last token's dS term, decay 0")
+    assert np.array_equal(ds0[:, 0], np.zeros_like(ds0[:, 0])), "dS0 must vanish at decay 0"
+
 
 def check_backward_empty_sequence(o):
     """N = 0: no gradients of the sequence; the starting state's gradient is dS."""
@@ -478,5 +507,6 @@ ALL_CHECKS = [
     check_backward_euler_identities,
     check_backward_gamma_one_is_library_autograd,
     check_backward_scans_are_forward_retentions,
+    check_backward_zero_decay_as_forwards,
     check_backward_empty_sequence,
 ]

@@ -3,7 +3,11 @@
 // next phase starts, which is what the kernel's barriers guarantee on the
 // GPU.  Shared memory is a heap buffer of exactly the kernel's dynamic size,
 // filled with NaN, so an out-of-range index shows up under AddressSanitizer
-// and a read of a slot no phase wrote shows up as a non-finite gradient.
+// and a read of a slot no phase wrote shows up as a non-finite gradient.  The
+// per-chunk regions (a rows, b rows, the transposed w slab and the scores)
+// are filled with NaN again before every chunk's load phase, so a phase that
+// reads a slot of the current chunk it did not write cannot pick up the
+// previous chunk's value; the state slab and the power table carry over.
 // This is test code: the library never runs its kernels on the CPU.
 //
 // Input file: int32 header {bf16, B, H, N, dk, dv, has_state_in, has_dstate},
@@ -30,9 +34,11 @@ void step_all(const BwdArgs& p, int BH) {
       const BwdSmem<C> s(smem, p.wmax);
       for (int t = 0; t < kBwdThreads; ++t) bwd_init<C>(p, r, s, t);
       const int n_chunks = (p.N + C - 1) / C;
+      const size_t per_chunk = (size_t)(s.St - s.As);  // As, Bs, WT and P, contiguous
       for (int it = 0; it < n_chunks; ++it) {
         const int s0 = (r.fwd ? it : n_chunks - 1 - it) * C;
         const int L = imin(C, p.N - s0);
+        for (size_t i = 0; i < per_chunk; ++i) s.As[i] = __builtin_nanf("");
         for (int t = 0; t < kBwdThreads; ++t) bwd_load<C, T>(p, r, s, s0, L, t);
         for (int t = 0; t < kBwdThreads; ++t) bwd_scores<C>(r, s, L, t);
         for (int t = 0; t < kBwdThreads; ++t) bwd_rows<C, T>(p, r, s, s0, L, t);

@@ -134,22 +134,35 @@ def test_chunkwise_groupnorm_validation(lib):
 def test_backward_validation(lib):
     """Host checks of the gradient call: required pointers present and
     aligned, the starting-state gradient not written over dstate or state_in,
-    widths above 512 or not a multiple of 4 refused."""
+    no gradient overlapping an input or another gradient, widths above 512
+    or not a multiple of 4 refused."""
+    # distinct, non-overlapping fake device addresses (never dereferenced)
+    Q, K, V, G, DO, DQ, DK, DV = (ctypes.c_void_p((i + 1) << 32) for i in range(8))
     P2, P3 = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
     for fn in (lib.retention_backward, lib.retention_backward_f32):
         # (q, k, v, gamma, state_in, dout, dstate, dq, dk, dv, dstate_in, B, H, N, dk, dv, stream)
-        assert fn(None, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, None, None, P, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, P, None, None, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, P, None, P, P, P_ODD, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, P_ODD, P, None, P, P, P, None, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, P, P2, P, P, P, P2, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, P3, P, P2, P, P, P, P3, 1, 1, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 0, 8, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, -1, 64, 64, None) == binding.RET_ERR_INVALID
-        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 64, 640, None) == binding.RET_ERR_UNSUPPORTED
-        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 1024, 64, None) == binding.RET_ERR_UNSUPPORTED
-        assert fn(P, P, P, P, None, P, None, P, P, P, None, 1, 1, 8, 66, 64, None) == binding.RET_ERR_UNSUPPORTED
+        def call(q=Q, k=K, v=V, gm=G, s0=None, do=DO, ds=None, dq=DQ, dk_=DK, dv_=DV, ds0=None,
+                 B=1, H=1, N=8, dk=64, dv=64):
+            return fn(q, k, v, gm, s0, do, ds, dq, dk_, dv_, ds0, B, H, N, dk, dv, None)
+        assert call(q=None) == binding.RET_ERR_INVALID
+        assert call(do=None) == binding.RET_ERR_INVALID
+        assert call(dq=None) == binding.RET_ERR_INVALID
+        assert call(dv_=P_ODD) == binding.RET_ERR_INVALID
+        assert call(s0=P_ODD) == binding.RET_ERR_INVALID
+        assert call(ds=P2, ds0=P2) == binding.RET_ERR_INVALID
+        assert call(s0=P3, ds=P2, ds0=P3) == binding.RET_ERR_INVALID
+        assert call(H=0) == binding.RET_ERR_INVALID
+        assert call(N=-1) == binding.RET_ERR_INVALID
+        # a gradient written over an input, or over another gradient, in whole or in part
+        for bad in (dict(dq=Q), dict(dk_=K), dict(dv_=V), dict(dv_=DO), dict(dq=DO), dict(dk_=DQ),
+                    dict(dv_=ctypes.c_void_p(Q.value + 16)), dict(dq=ctypes.c_void_p(DV.value + 512))):
+            assert call(**bad) == binding.RET_ERR_INVALID, bad
+        # adjacent but disjoint ranges are fine (fails only later, on the width)
+        q_bytes = 8 * 64 * (2 if fn is lib.retention_backward else 4)
+        assert call(dq=ctypes.c_void_p(Q.value + q_bytes), dk=64, dv=640) == binding.RET_ERR_UNSUPPORTED
+        assert call(dv=640) == binding.RET_ERR_UNSUPPORTED
+        assert call(dk=1024) == binding.RET_ERR_UNSUPPORTED
+        assert call(dk=66) == binding.RET_ERR_UNSUPPORTED
         # nothing to do: no tokens and no starting-state gradient wanted
         assert fn(None, None, None, None, None, None, None, None, None, None, None, 1, 1, 0, 64, 64, None) == \
             binding.RET_OK

@@ -37,7 +37,7 @@ def _rank_main(rank, world, port, out_dir):
     import torch.distributed as dist
 
     import bench
-    w, r, local = bench.dist_setup()
+    w, r, local = bench.dist_setup(backend="gloo")  # the same backend on every machine
     bench.barrier(w)
     local_ms = 10.0 + 5.0 * rank          # rank 1 is the slow one
     slowest = bench.max_over_ranks(local_ms, w, torch.device("cpu"))
