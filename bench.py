@@ -1,29 +1,35 @@
 """Benchmark of the retention hot path on B300.
 
 Headline: chunkwise-forward tokens/s (B*N sequence positions per second, all
-heads included) on the mid workload B=4, H=8, N=2048, d_k=d_v=128, chunk=64,
-bf16 q/k/v/out with fp32 accumulation and state.  One step = one
-retention_chunkwise call over one batch; inputs are resident in HBM and L2 is
-flushed between timed steps, outside the timed events: a 512 MiB write, then
-a 512 MiB read, so that neither the inputs nor the flush's own dirty lines
-(whose write-back would land inside the timed call) remain in L2.
+heads included) on the 7B-shaped workload B=8, H=16, N=8192, d_k=256,
+d_v=512, chunk=128 (the largest single-GPU workload), bf16 q/k/v/out with
+fp32 accumulation and state.  One step = one retention_chunkwise call over
+one batch; inputs are resident in HBM and L2 is flushed between timed steps,
+outside the timed events: a 512 MiB write, then a 512 MiB read, so that
+neither the inputs nor the flush's own dirty lines (whose write-back would
+land inside the timed call) remain in L2.
 
 Also reported on the same line:
-  decode      the recurrent decode step on 64 sequences x 16 heads, d_k=128,
-              d_v=256, fp32 state (128 MiB > L2): 1024 sequential steps
-              captured in one CUDA graph; steps/s and HBM roofline.
-  workloads   the long-context (B=1,H=16,N=16384,d_k=128,d_v=256,C=128) and
-              7B-shaped (B=8,H=16,N=8192,d_k=256,d_v=512,C=128) chunkwise runs.
   e2e         the headline metric through host buffers: pinned host q/k/v
               copied in, the call, out and state copied back, per step.
   roofline    algorithmic bytes of one retention_chunkwise call (Q,K,V read,
               out and final state written) over its CUDA-event duration,
-              against the measured HBM copy bandwidth.
+              against the measured HBM copy bandwidth; the tensor fraction
+              (algorithmic flops over the measured bf16 peak) beside it.
   cpu_baseline  the fp64 CPU oracle (chunkwise form, same chunk) on the host
-              cores, timed on the full mid workload.
+              cores, timed on one batch row of the workload (all its heads)
+              and scaled to the whole batch.
+  mid, long   the mid (B=4,H=8,N=2048,d_k=d_v=128,C=64) and long-context
+              (B=1,H=16,N=16384,d_k=128,d_v=256,C=128) chunkwise runs, each
+              with its own roofline and e2e.
+  decode      the recurrent decode step on 64 sequences x 16 heads, d_k=128,
+              d_v=256, fp32 state (128 MiB > L2): 1024 sequential steps
+              captured in one CUDA graph; steps/s and HBM roofline.
+  groupnorm, rotate, mid_groupnorm_fused, mid_backward   the other kernels.
 
 `--impl reference` times the fp64 CPU oracle alone on the same workload and
-metric (the full mid workload per step) and prints its own line.
+metric (one batch row of the 7B-shaped workload per step, scaled to the
+batch) and prints its own line.
 `--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b}`
 runs one workload alone and prints its timing
 (used to give ncu a small, single-workload command).
@@ -97,8 +103,13 @@ def decode_bytes(w) -> int:
     return B * H * (8 * dk * dv + 2 * (2 * dk + dv) + 2 * dv)
 
 
-def kernel_sha() -> str:
-    path = os.path.join(ROOT, "linear_attention_sequence_02_b300", "csrc", "chunk_tc.cu")
+# The source file of the kernel each workload's traffic was captured on.
+TRAFFIC_SOURCE = {"decode_step": "simt.cu", "groupnorm": "groupnorm.cu", "rotate": "rotate.cu"}
+
+
+def kernel_sha(workload: str = "mid") -> str:
+    name = TRAFFIC_SOURCE.get(workload, "chunk_tc.cu")
+    path = os.path.join(ROOT, "linear_attention_sequence_02_b300", "csrc", name)
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
@@ -107,7 +118,7 @@ def recorded_traffic(workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    sha = kernel_sha()
+    sha = kernel_sha(workload)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -486,23 +497,52 @@ def time_backward(w, reps, dev, flush, seed=0):
     return times
 
 
-def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
-    """fp64 oracle (chunkwise form, same chunk) on the full workload, repeated for >= min_seconds."""
-    import oracle
+def oracle_sample(w, seed=0):
+    """One batch row of workload `w` (all H heads) as fp64 arrays for the oracle."""
     from linear_attention_sequence_02_b300 import binding, inputs
-    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
-    q, k, v = inputs.qkv(B, H, N, dk, dv, 0, torch.bfloat16)
-    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    H, N, dk, dv = w["H"], w["N"], w["dk"], w["dv"]
+    q, k, v = inputs.qkv(1, H, N, dk, dv, seed, torch.bfloat16)
     g = binding.gamma_schedule(H).double().numpy()
+    return tuple(x.double().numpy() for x in (q, k, v)) + (g,)
+
+
+def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
+    """fp64 oracle (chunkwise form, same chunk) on one batch row of the
+    workload (all its heads), repeated for >= min_seconds; tokens/s of the
+    whole batch = B*N / (B * seconds per row)."""
+    import oracle
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    qd, kd, vd, g = oracle_sample(w)
     orc = oracle.default()
     passes, t0 = 0, time.perf_counter()
     while passes < max_passes and (time.perf_counter() - t0) < min_seconds:
         orc.chunkwise(qd, kd, vd, g, C)
         passes += 1
     dt = (time.perf_counter() - t0) / passes
-    return {"value": round(B * N / dt, 1), "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
-            "sample": f"full {w['name']} workload (B={B},H={H},N={N},dk={dk},dv={dv},chunk={C}), "
-                      f"{passes} fp64 passes, {dt:.3f} s each"}
+    return {"value": round(N / dt, 1), "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": f"one batch row of the {w['name']} workload (H={H},N={N},dk={dk},dv={dv},chunk={C}, "
+                      f"all {H} heads) per pass, {passes} fp64 passes of {dt:.3f} s; scaled to B={B} rows"}
+
+
+def chunkwise_entry(w, steps, warmup, dev, flush, hbm, tflops, peak_kind, rank=0):
+    """Device-timed chunkwise call on workload `w`: per-call times, rate, roofline."""
+    times, launches, how = time_chunkwise(w, steps, warmup, dev, flush, seed=rank)
+    avg_s = sum(times) / len(times) / 1e3
+    achieved = chunk_bytes(w) / avg_s / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": recorded_traffic(w["name"]),
+                "peak_kind": peak_kind, "kernel": "retention_chunkwise call (every launch of one call)",
+                "algorithmic_bytes_per_call": chunk_bytes(w),
+                "tensor_flops_frac": round(chunk_flops(w) / avg_s / 1e12 / tflops, 4)}
+    cfg = {k: w[k] for k in ("B", "H", "N", "dk", "dv", "chunk")}
+    return times, launches, how, roofline, cfg
+
+
+def e2e_entry(w, steps, warmup, dev, world=1, rank=0):
+    e2e_ms, h2d, d2h = time_e2e(w, steps, warmup, dev, seed=rank)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    return {"value": round(whole_job_rate(w["B"] * w["N"], world, e2e_ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 def run_ours(args):
@@ -514,35 +554,34 @@ def run_ours(args):
     hbm, tflops, peak_kind = peaks()
     flush = L2Flush(dev)
 
-    # ---- headline: mid chunkwise, device-timed ----
-    w = MID
+    # ---- headline: 7B-shaped chunkwise, device-timed ----
+    w = B7
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        times, launches, how = time_chunkwise(w, args.steps, args.warmup, dev, flush, seed=rank)
+        times, launches, how, roofline, cfg = chunkwise_entry(w, args.steps, args.warmup, dev, flush, hbm, tflops,
+                                                              peak_kind, rank)
     torch.cuda.synchronize(dev)
     barrier(world)
     total_ms = max_over_ranks(sum(times), world, dev)
     ms = total_ms / args.steps
     value = whole_job_rate(w["B"] * w["N"] * args.steps, world, total_ms / 1e3)
-    avg_s = sum(times) / len(times) / 1e3
-    achieved = chunk_bytes(w) / avg_s / 1e9
-    traffic = recorded_traffic(w["name"])
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": traffic,
-                "peak_kind": peak_kind, "kernel": "retention_chunkwise call (pre-pass + main)",
-                "algorithmic_bytes_per_call": chunk_bytes(w),
-                "tensor_flops_frac": round(chunk_flops(w) / avg_s / 1e12 / tflops, 4)}
 
     # ---- e2e through host buffers ----
-    e2e_ms, h2d, d2h = time_e2e(w, max(3, args.steps // 2), max(3, args.warmup), dev, seed=rank)
-    e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    e2e = {"value": round(whole_job_rate(w["B"] * w["N"], world, e2e_ms / 1e3), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    e2e = e2e_entry(w, max(3, args.steps // 4), 3, dev, world, rank)
 
     extra = {}
-    # ---- decode step ----
     if not args.quick:
+        # ---- the other chunkwise workloads ----
+        for wl in (MID, LONG):
+            t, n, h, rf, c = chunkwise_entry(wl, args.steps, 3, dev, flush, hbm, tflops, peak_kind, rank)
+            a_s = statistics.median(t) / 1e3
+            extra[wl["name"]] = {
+                "tokens_per_s": round(wl["B"] * wl["N"] / a_s, 1), "ms_per_call": round(a_s * 1e3, 5),
+                "config": c | {"l2": "flushed between timed calls (512 MiB write, then 512 MiB read)", "timing": h},
+                "roofline": rf, "e2e": e2e_entry(wl, max(3, args.steps // 2), 3, dev, world, rank),
+                "gpu_launches": n}
+        # ---- decode step ----
         dt = time_decode(DECODE, 3, dev)
         step_ms = statistics.median(dt)
         bytes_step = decode_bytes(DECODE)
@@ -579,56 +618,45 @@ def run_ours(args):
             "config": {k: rw[k] for k in ("B", "H", "N", "d")} | {"l2": "flushed before each call (512 MiB write, then 512 MiB read)",
                                                                   "timing": "CUDA events per call"},
             "roofline": {"bound": "hbm", "achieved": round(rbytes / rt / 1e9, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(rbytes / rt / 1e9 / hbm, 4), "traffic": None},
+                         "frac": round(rbytes / rt / 1e9 / hbm, 4), "traffic": recorded_traffic("rotate")},
             "gpu_launches": 1}
         # chunkwise with the GroupNorm fused into its epilogue, on the mid workload
-        tf, nf, _ = time_chunkwise(w, args.steps, 3, dev, flush, norm=True)
+        mid_ms = extra["mid"]["ms_per_call"]
+        tf, nf, _ = time_chunkwise(MID, args.steps, 3, dev, flush, norm=True)
         f_s = statistics.median(tf) / 1e3
         extra["mid_groupnorm_fused"] = {
-            "tokens_per_s": round(w["B"] * w["N"] / f_s, 1), "ms_per_call": round(f_s * 1e3, 5),
-            "separate_ms": round(ms + gt * 1e3, 5),
+            "tokens_per_s": round(MID["B"] * MID["N"] / f_s, 1), "ms_per_call": round(f_s * 1e3, 5),
+            "separate_ms": round(mid_ms + gt * 1e3, 5),
             "config": {"workload": "mid retention chunkwise fwd + GroupNorm over each head (fused epilogue)",
                        "out_layout": "[B, N, H, dv]"},
             "gpu_launches": nf}
-        # gradients of the mid workload (CUDA-core fp32 kernel, one launch)
-        bt = statistics.median(time_backward(w, 10, dev, flush)) / 1e3
+        # gradients of the mid workload
+        bt = statistics.median(time_backward(MID, 10, dev, flush)) / 1e3
         props = torch.cuda.get_device_properties(dev)
         max_mhz = clk.summary().get("sm_max_mhz") or 2032
         fp32_peak = props.multi_processor_count * 128 * 2 * max_mhz * 1e6 / 1e12
-        bflops = backward_flops(w, backward_chunk(w["dk"], w["dv"]))
+        bflops = backward_flops(MID, backward_chunk(MID["dk"], MID["dv"]))
         extra["mid_backward"] = {
-            "tokens_per_s": round(w["B"] * w["N"] / bt, 1), "ms_per_call": round(bt * 1e3, 5),
-            "config": {"workload": "mid retention gradients (dq, dk, dv), no states", "B": w["B"], "H": w["H"],
-                       "N": w["N"], "dk": w["dk"], "dv": w["dv"],
-                       "internal_chunk": backward_chunk(w["dk"], w["dv"]),
+            "tokens_per_s": round(MID["B"] * MID["N"] / bt, 1), "ms_per_call": round(bt * 1e3, 5),
+            "config": {"workload": "mid retention gradients (dq, dk, dv), no states", "B": MID["B"], "H": MID["H"],
+                       "N": MID["N"], "dk": MID["dk"], "dv": MID["dv"],
+                       "internal_chunk": backward_chunk(MID["dk"], MID["dv"]),
                        "l2": "flushed before each call (512 MiB write, then 512 MiB read)"},
             "roofline": {"bound": "alu", "achieved": round(bflops / bt / 1e12, 2),
                          "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
                          "peak_kind": "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock",
                          "frac": round(bflops / bt / 1e12 / fp32_peak, 4), "traffic": None,
-                         "hbm_frac": round(backward_bytes(w) / bt / 1e9 / hbm, 4)},
+                         "hbm_frac": round(backward_bytes(MID) / bt / 1e9 / hbm, 4)},
             "gpu_launches": 1}
-        for wl in (LONG, B7):
-            t, n, _ = time_chunkwise(wl, max(3, args.steps // 4), 3, dev, flush)
-            a_s = statistics.median(t) / 1e3
-            ach = chunk_bytes(wl) / a_s / 1e9
-            extra[wl["name"]] = {
-                "tokens_per_s": round(wl["B"] * wl["N"] / a_s, 1), "ms_per_call": round(a_s * 1e3, 4),
-                "config": {k: wl[k] for k in ("B", "H", "N", "dk", "dv", "chunk")},
-                "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                             "frac": round(ach / hbm, 4), "traffic": recorded_traffic(wl["name"]),
-                             "tensor_flops_frac": round(chunk_flops(wl) / a_s / 1e12 / tflops, 4)},
-                "gpu_launches": n}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded iid N(0,1) q,k,v)",
-        "config": {"workload": "mid retention chunkwise fwd", "B": w["B"], "H": w["H"], "N": w["N"],
-                   "dk": w["dk"], "dv": w["dv"], "chunk": w["chunk"], "global_batch": w["B"] * world,
+        "config": {"workload": "7B-shaped retention chunkwise fwd", **cfg, "global_batch": w["B"] * world,
                    "seq_len": w["N"], "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)",
+                   "l2": "flushed between timed steps (512 MiB write, then 512 MiB read); inputs 3.2 GB > L2",
                    "timing": how},
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -652,26 +680,25 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    from linear_attention_sequence_02_b300 import inputs
-    w = MID
+    w = B7
     B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
-    q, k, v = inputs.qkv(B, H, N, dk, dv, 0, torch.bfloat16)
-    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
-    g = [oracle.gamma(h) for h in range(H)]
+    qd, kd, vd, g = oracle_sample(w)
     orc = oracle.default()
     for _ in range(args.warmup):
         orc.chunkwise(qd, kd, vd, g, C)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         orc.chunkwise(qd, kd, vd, g, C)
-    full_s = (time.perf_counter() - t0) / args.steps
+    row_s = (time.perf_counter() - t0) / args.steps
+    full_s = row_s * B  # the whole batch is B such rows
     value = B * N / full_s
-    sample = f"full mid workload per step (all {B * H} heads), fp64 chunkwise form, chunk {C}"
+    sample = (f"one batch row of the 7B-shaped workload per step (all {H} heads, N={N}), fp64 chunkwise "
+              f"form, chunk {C}; scaled to the B={B} rows of the workload")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(full_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded iid N(0,1) q,k,v)",
-            "config": {"workload": "mid retention chunkwise fwd", "B": B, "H": H, "N": N, "dk": dk,
+            "config": {"workload": "7B-shaped retention chunkwise fwd", "B": B, "H": H, "N": N, "dk": dk,
                        "dv": dv, "chunk": C, "global_batch": B, "seq_len": N,
                        "parallelism": "host cores (OpenMP over heads)"},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": orc.threads(),
@@ -691,7 +718,9 @@ def run_only(args):
         return
     flush = L2Flush(dev)
     if args.only in ("backward", "backward_long", "backward_7b"):
-        wl = {"backward": MID, "backward_long": LONG, "backward_7b": B7}[args.only]
+        wl = dict({"backward": MID, "backward_long": LONG, "backward_7b": B7}[args.only])
+        if args.batch:
+            wl["B"] = args.batch
         t = time_backward(wl, args.steps, dev, flush)
         print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps,
                           "tokens_per_s": round(wl["B"] * wl["N"] / (statistics.median(t) / 1e3), 1)}))
@@ -701,9 +730,12 @@ def run_only(args):
         t = fn(wl, args.steps, dev, flush)
         print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps}))
         return
-    w = {"mid": MID, "long": LONG, "7b": B7}[args.only]
+    w = dict({"mid": MID, "long": LONG, "7b": B7}[args.only])
+    if args.batch:
+        w["B"] = args.batch  # a smaller case of the same shape (e.g. for an ncu capture)
     t, n, how = time_chunkwise(w, args.steps, args.warmup, dev, flush)
-    print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": n, "timing": how}))
+    print(json.dumps({"only": args.only, "B": w["B"], "ms_per_call": statistics.median(t), "launches": n,
+                      "timing": how}))
 
 
 def main():
@@ -714,6 +746,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="with --only: batch rows instead of the workload's")
     ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate", "backward", "backward_long",
                                        "backward_7b"], default=None)
     args = ap.parse_args()

@@ -82,8 +82,14 @@ typedef enum {
  * zero.  If state_out is not NULL it receives the state after token N-1
  * (zero when N == 0).
  *
- * Supported: chunk in {64, 128}; dk in {128, 256}; dv a multiple of 64
- * (at most 1024); N >= 0.  Other shapes return RET_ERR_UNSUPPORTED.  When the
+ * Supported: chunk in {32, 64, 128}; dk a multiple of 16 in [16, 256]; dv a
+ * multiple of 16 in [16, 1024]; N >= 0.  Other shapes return
+ * RET_ERR_UNSUPPORTED.  The chunk length is a tiling choice that does not
+ * change the result (every chunk length computes the same sums, up to
+ * rounding order); chunk 32 runs on 64-token tiles, the tensor cores'
+ * smallest tile height.  Widths below the kernel's tile (128 or 256 query
+ * and key columns, 64 or 128 value columns) are padded with zeros by the
+ * loads, which leaves every product unchanged.  When the
  * call splits the sequence into segments to fill the GPU it allocates a
  * float32 scratch buffer stream-ordered (cudaMallocAsync / cudaFreeAsync on
  * `stream`); retention_chunkwise_ws takes a caller-provided buffer instead.
@@ -297,9 +303,17 @@ int retention_step_f32(const float *q, const float *k, const float *v, float *st
  * one another: a gradient whose bytes overlap q, k, v, dout or another
  * gradient, or dstate_in equal to dstate or state_in, returns
  * RET_ERR_INVALID.  When N == 0, dstate_in receives a copy of dstate (zero if
- * NULL).  Arithmetic is float32 on the CUDA cores, one launch, no workspace.
- * Supported: dk, dv multiples of 4, at most 512; other widths return
- * RET_ERR_UNSUPPORTED.
+ * NULL).
+ * How it runs: with bf16 tensors and dk, dv multiples of 16 in [16, 256], on
+ * the tensor cores, each gradient as a chunkwise forward of permuted
+ * operands (dq the forward of (dout, v, k) from S0^T; dk and dv the
+ * time-reversed forwards of (v, dout, q) and (k, q, dout) from dstate^T/(s g)
+ * and dstate/(s g); dS0 = s g times the final state of the latter), with bf16
+ * operands and float32 accumulation and state, and a stream-ordered scratch
+ * buffer (cudaMallocAsync / cudaFreeAsync on `stream`) for the permuted
+ * operands.  Otherwise (other widths, or the float32 twin) float32 arithmetic
+ * on the CUDA cores, one launch, no workspace.  Supported: dk, dv multiples of
+ * 4, at most 512; other widths return RET_ERR_UNSUPPORTED.
  * retention_backward_f32 is the same with float32 q/k/v/dout/dq/dk/dv.
  */
 int retention_backward(const void *q, const void *k, const void *v, const float *gamma,
@@ -310,6 +324,14 @@ int retention_backward_f32(const float *q, const float *k, const float *v, const
                            const float *state_in, const float *dout, const float *dstate,
                            float *dq, float *dk_out, float *dv_out, float *dstate_in,
                            int B, int H, int N, int dk, int dv, void *stream);
+
+/*
+ * retention_backward_launches -- number of kernels one bf16 retention_backward
+ * call with these sizes enqueues (for launch accounting); the flags say
+ * whether state_in and dstate are given and dstate_in is wanted.  Host only.
+ */
+int retention_backward_launches(int B, int H, int N, int dk, int dv, int has_state_in, int has_dstate,
+                                int want_dstate_in, int *launches);
 
 /*
  * retention_gamma_schedule -- host function: gamma_out[h] = 1 - 2^(-5-h),

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "retention_rotate": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
     "retention_backward": [_vp] * 11 + [_i] * 5 + [_vp],
     "retention_backward_f32": [_vp] * 11 + [_i] * 5 + [_vp],
+    "retention_backward_launches": [_i] * 8 + [ctypes.POINTER(_i)],
     "retention_step": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_step_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_gamma_schedule": [_i, _fp],
@@ -336,6 +337,16 @@ def retention_backward(q, k, v, gamma, dout, dstate=None, state_in=None, want_ds
     dstate_in None when not wanted.  `grads` may pass the four output tensors."""
     return _backward("retention_backward", torch.bfloat16, q, k, v, gamma, dout, dstate, state_in,
                      want_dstate_in, grads, stream)
+
+
+def backward_launches(B: int, H: int, N: int, dk: int, dv: int, has_state_in: bool = False,
+                      has_dstate: bool = False, want_dstate_in: bool = False) -> int:
+    """Kernels one bf16 retention_backward call with these sizes enqueues."""
+    n = _i(0)
+    _check("retention_backward_launches",
+           lib().retention_backward_launches(B, H, N, dk, dv, int(has_state_in), int(has_dstate),
+                                             int(want_dstate_in), ctypes.byref(n)))
+    return n.value
 
 
 def retention_backward_f32(q, k, v, gamma, dout, dstate=None, state_in=None, want_dstate_in: bool = True,

@@ -86,7 +86,8 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
   if (sms <= 0) return RET_ERR_CUDA;
   st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
   if (st != RET_OK) return st;
-  if (norm && plan.n_dv_tiles != 1) return RET_ERR_UNSUPPORTED;  // a head's row must fit one CTA
+  // GroupNorm: a head's whole row, unpadded, in one CTA (dv of 64 or 128)
+  if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv)) return RET_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) {
     // the state after no tokens is the state before them
@@ -100,8 +101,8 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
     if (cudaMallocAsync(reinterpret_cast<void**>(&ws), plan.workspace_bytes, s) != cudaSuccess)
       return RET_ERR_CUDA;
   }
-  cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv,
-                                       chunk, plan, ws, norm, s);
+  cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, plan, ws,
+                                       norm, 0.f, s);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = e2;
@@ -147,6 +148,9 @@ int backward_call(bool bf16, const void* q, const void* k, const void* v, const 
     return from_cuda(cudaMemcpyAsync(dstate_in, dstate, sizeof(float) * (size_t)B * H * dk * dv,
                                      cudaMemcpyDeviceToDevice, s));
   }
+  if (bf16 && ret::backward_tc_supported(dk, dv))
+    return from_cuda(ret::launch_backward_tc(q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out, dstate_in, B,
+                                             H, N, dk, dv, s));
   return from_cuda(ret::launch_backward(bf16, q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out,
                                         dstate_in, B, H, N, dk, dv, s));
 }
@@ -220,8 +224,8 @@ int retention_chunkwise_ws(const void* q, const void* k, const void* v, const fl
     if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256))
       return RET_ERR_INVALID;
   }
-  return from_cuda(ret::launch_chunk_tc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv,
-                                        chunk, plan, static_cast<float*>(workspace), nullptr, s));
+  return from_cuda(ret::launch_chunk_tc(q, k, v, gamma, nullptr, out, state_out, B, H, N, dk, dv, plan,
+                                        static_cast<float*>(workspace), nullptr, 0.f, s));
 }
 
 int retention_chunkwise(const void* q, const void* k, const void* v, const float* gamma, void* out,
@@ -316,6 +320,23 @@ int retention_backward(const void* q, const void* k, const void* v, const float*
                        void* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv, void* stream) {
   return backward_call(true, q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out, dstate_in, B, H, N, dk,
                        dv, stream);
+}
+
+int retention_backward_launches(int B, int H, int N, int dk, int dv, int has_state_in, int has_dstate,
+                                int want_dstate_in, int* launches) {
+  if (!launches || B <= 0 || H <= 0 || N < 0 || dk <= 0 || dv <= 0) return RET_ERR_INVALID;
+  if (N == 0) {
+    *launches = want_dstate_in ? 1 : 0;
+    return RET_OK;
+  }
+  if (!ret::backward_tc_supported(dk, dv)) {
+    *launches = 1;
+    return RET_OK;
+  }
+  const int n = ret::backward_tc_launches(B, H, N, dk, dv, has_state_in != 0, has_dstate != 0, want_dstate_in != 0);
+  if (n < 0) return RET_ERR_UNSUPPORTED;
+  *launches = n;
+  return RET_OK;
 }
 
 int retention_backward_f32(const float* q, const float* k, const float* v, const float* gamma,

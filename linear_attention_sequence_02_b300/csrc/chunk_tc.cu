@@ -186,7 +186,8 @@ struct TcParams {
   const float* norm_b;  //   (null: one, zero) and eps
   float norm_eps;
   int H, N, dv, n_dv_tiles, BH, segments, seg_chunks, n_chunks;
-  float scale;       // 1/sqrt(dk)
+  int dk;            // query/key width (<= DK; the columns past it are zero-filled by the loads)
+  float scale;       // factor of the query (1/sqrt(dk) unless the caller sets another)
 };
 
 __device__ __forceinline__ float gamma_pow(float g, float lg, float d) {
@@ -387,9 +388,10 @@ __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, u
   if (to_out) {
     __syncthreads();
     const float4* src = reinterpret_cast<const float4*>(sm);
-    float* base = p.state_out + (size_t)bh * DK * p.dv + dv0;
-    for (int q4 = threadIdx.x; q4 < DK * DVT / 4; q4 += kThreads) {
-      const int row = q4 / (DVT / 4), c4 = q4 % (DVT / 4);
+    float* base = p.state_out + (size_t)bh * p.dk * p.dv + dv0;
+    const int cols4 = min(DVT, p.dv - dv0) / 4;  // value columns of this tile inside dv
+    for (int q4 = threadIdx.x; q4 < p.dk * cols4; q4 += kThreads) {
+      const int row = q4 / cols4, c4 = q4 % cols4;
       *reinterpret_cast<float4*>(base + (size_t)row * p.dv + 4 * c4) = src[row * (L::kStageRow / 4) + c4];
     }
   }
@@ -465,14 +467,16 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         float acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-        if (p.state_in != nullptr) {
+        const int row = hh * 128 + srow;
+        if (p.state_in != nullptr && row < p.dk) {
           // gamma^(seg Lseg) state_in, row hh*128 + srow, columns dv0 + 32 cb ..
+          // (rows past dk and columns past dv are padding: they stay zero)
           const float f = gamma_pow(g, lg, (float)seg * seg_len);
-          const float4* src = reinterpret_cast<const float4*>(
-              p.state_in + ((size_t)bh * DK + hh * 128 + srow) * p.dv + dv0 + cb * 32);
+          const int col = dv0 + cb * 32;
+          const float4* src = reinterpret_cast<const float4*>(p.state_in + ((size_t)bh * p.dk + row) * p.dv + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 x = __ldg(src + j);
+            const float4 x = col + 4 * j < p.dv ? __ldg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             acc[4 * j + 0] = f * x.x;
             acc[4 * j + 1] = f * x.y;
             acc[4 * j + 2] = f * x.z;
@@ -1267,14 +1271,19 @@ int pick_dvt(int dv) { return dv % 128 == 0 ? 128 : 64; }
 }  // namespace
 
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan) {
-  if (!(chunk == 64 || chunk == 128)) return false;
-  if (!(dk == 128 || dk == 256)) return false;
-  if (dv <= 0 || dv % 64 != 0 || dv > 1024) return false;
+  // chunk 32 runs on 64-token tiles: the chunk length is a tiling choice that
+  // leaves the result unchanged (every chunk length computes the same sums),
+  // and the tensor cores' smallest tile has 64 rows.
+  if (!(chunk == 32 || chunk == 64 || chunk == 128)) return false;
+  if (dk < 16 || dk > 256 || dk % 16 != 0) return false;
+  if (dv < 16 || dv > 1024 || dv % 16 != 0) return false;
   if (N < 0) return false;
   const int dvt = pick_dvt(dv);
+  plan->chunk = chunk == 32 ? 64 : chunk;
+  plan->dk_tile = dk <= 128 ? 128 : 256;
   plan->dvt = dvt;
-  plan->n_dv_tiles = dv / dvt;
-  plan->n_chunks = (N + chunk - 1) / chunk;
+  plan->n_dv_tiles = (dv + dvt - 1) / dvt;
+  plan->n_chunks = (N + plan->chunk - 1) / plan->chunk;
   const long long units = (long long)B * H * plan->n_dv_tiles;
   if (units > (1LL << 30)) return false;
   // Enough segments that every SM gets a CTA, each segment at least 4 chunks.
@@ -1285,8 +1294,10 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   if (plan->n_chunks > 0) segs = (plan->n_chunks + seg_chunks - 1) / seg_chunks;  // no empty segment
   plan->segments = std::max(1, segs);
   plan->seg_chunks = std::max(1, seg_chunks);
-  plan->workspace_bytes =
-      plan->segments > 1 ? sizeof(float) * (size_t)B * H * (plan->segments - 1) * dk * dv : 0;
+  // segment states cover the padded tile (dk_tile rows, n_dv_tiles * dvt columns)
+  plan->workspace_bytes = plan->segments > 1 ? sizeof(float) * (size_t)B * H * (plan->segments - 1) *
+                                                   plan->dk_tile * (size_t)plan->n_dv_tiles * dvt
+                                             : 0;
   plan->launches = plan->segments > 1 ? 2 : 1;
   if ((long long)units * plan->segments > INT32_MAX) return false;
   return true;
@@ -1294,10 +1305,12 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H, int N,
-                            int dk, int dv, int chunk, const ChunkPlan& plan, float* workspace,
-                            const ChunkNorm* norm, cudaStream_t s) {
+                            int dk, int dv, const ChunkPlan& plan, float* workspace,
+                            const ChunkNorm* norm, float scale, cudaStream_t s) {
   const int BH = B * H;
-  if (norm && plan.n_dv_tiles != 1) return cudaErrorNotSupported;  // a row must fit one CTA
+  const int chunk = plan.chunk;
+  // GroupNorm statistics need a head's whole row, unpadded, in one CTA
+  if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv)) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, q, dk, N, BH, chunk) || !make_map(&mk, k, dk, N, BH, chunk) ||
       !make_map(&mv, v, dv, N, BH, chunk) ||
@@ -1314,32 +1327,34 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.H = H;
   p.N = N;
   p.dv = dv;
+  p.dk = dk;
   p.n_dv_tiles = plan.n_dv_tiles;
   p.BH = BH;
   p.segments = plan.segments;
   p.seg_chunks = plan.seg_chunks;
   p.n_chunks = plan.n_chunks;
-  p.scale = (float)(1.0 / std::sqrt((double)dk));
+  p.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)dk));
   const bool t128 = plan.dvt == 128;
+  const int dkt = plan.dk_tile;
   if (norm) {
-    if (chunk == 64 && dk == 128) return t128 ? launch_pair<64, 128, 128, true>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<64, 128, 64, true>(mq, mk, mv, mo, p, s);
-    if (chunk == 128 && dk == 128) return t128 ? launch_pair<128, 128, 128, true>(mq, mk, mv, mo, p, s)
-                                               : launch_pair<128, 128, 64, true>(mq, mk, mv, mo, p, s);
-    if (chunk == 64 && dk == 256) return t128 ? launch_pair<64, 256, 128, true>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<64, 256, 64, true>(mq, mk, mv, mo, p, s);
-    if (chunk == 128 && dk == 256) return t128 ? launch_pair<128, 256, 128, true>(mq, mk, mv, mo, p, s)
-                                               : launch_pair<128, 256, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, true>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<64, 128, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, true>(mq, mk, mv, mo, p, s)
+                                                : launch_pair<128, 128, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, true>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<64, 256, 64, true>(mq, mk, mv, mo, p, s);
+    if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, true>(mq, mk, mv, mo, p, s)
+                                                : launch_pair<128, 256, 64, true>(mq, mk, mv, mo, p, s);
     return cudaErrorNotSupported;
   }
-  if (chunk == 64 && dk == 128) return t128 ? launch_pair<64, 128, 128, false>(mq, mk, mv, mo, p, s)
-                                            : launch_pair<64, 128, 64, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dk == 128) return t128 ? launch_pair<128, 128, 128, false>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<128, 128, 64, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 64 && dk == 256) return t128 ? launch_pair<64, 256, 128, false>(mq, mk, mv, mo, p, s)
-                                            : launch_pair<64, 256, 64, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dk == 256) return t128 ? launch_pair<128, 256, 128, false>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<128, 256, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, false>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 128, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, false>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 128, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, false>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 256, 64, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, false>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 256, 64, false>(mq, mk, mv, mo, p, s);
   return cudaErrorNotSupported;
 }
 

@@ -30,8 +30,10 @@ cudaError_t launch_chunkwise_f32(const float* q, const float* k, const float* v,
 
 // ---- tensor-core chunkwise (chunk_tc.cu) --------------------------------------
 struct ChunkPlan {
+  int chunk;        // tokens per tile (64 or 128; a requested chunk of 32 runs as 64)
+  int dk_tile;      // query/key columns the kernel is built for (128 or 256; dk <= dk_tile)
   int dvt;          // value columns per CTA (64 or 128)
-  int n_dv_tiles;   // dv / dvt
+  int n_dv_tiles;   // ceil(dv / dvt); the last tile's columns past dv are padding
   int segments;     // sequence segments per head (>= 1)
   int seg_chunks;   // chunks per segment (all segments but the last are full)
   int n_chunks;     // ceil(N / chunk)
@@ -49,11 +51,12 @@ struct ChunkNorm {
   float eps;
 };
 // state_in (nullable) is the state before the first token, [B*H][dk][dv];
-// norm (nullable) selects the GroupNorm epilogue.
+// norm (nullable) selects the GroupNorm epilogue; scale multiplies the query
+// (<= 0: 1/sqrt(dk)).
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H,
-                            int N, int dk, int dv, int chunk, const ChunkPlan& plan,
-                            float* workspace, const ChunkNorm* norm, cudaStream_t s);
+                            int N, int dk, int dv, const ChunkPlan& plan, float* workspace,
+                            const ChunkNorm* norm, float scale, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 
 // ---- gradients of the forward on the CUDA cores (backward.cu) ------------------
@@ -64,6 +67,16 @@ size_t backward_smem_bytes(int dk, int dv);
 cudaError_t launch_backward(bool bf16, const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, const void* dout, const float* dstate, void* dq, void* dk_out,
                             void* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv, cudaStream_t s);
+
+// ---- gradients of the forward on the tensor cores (bwd_tc.cu) -----------------
+// Widths the tensor-core gradients handle (each gradient is a chunkwise
+// forward of permuted operands, so both widths must be forward widths).
+bool backward_tc_supported(int dk, int dv);
+cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, const float* gamma, const float* state_in,
+                               const void* dout, const float* dstate, void* dq, void* dk_out, void* dv_out,
+                               float* dstate_in, int B, int H, int N, int dk, int dv, cudaStream_t s);
+// Kernels one such call enqueues on a GPU with 148 SMs (-1: unsupported).
+int backward_tc_launches(int B, int H, int N, int dk, int dv, bool has_state_in, bool has_dstate, bool want_dstate_in);
 
 // ---- position phase rotation of queries and keys (rotate.cu) -------------------
 bool rotate_supported(int N, int d, int n0);

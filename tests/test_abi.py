@@ -73,6 +73,47 @@ def test_chunkwise_rejects_bad_arguments_on_host(lib, args, want):
     assert lib.retention_chunkwise_ws(*args, None, 0, None) == want
 
 
+@pytest.mark.parametrize("dk,dv,chunk,want", [
+    (128, 128, 64, binding.RET_OK),
+    (16, 16, 32, binding.RET_OK),              # narrowest widths, chunk 32
+    (256, 1024, 128, binding.RET_OK),          # widest
+    (192, 208, 64, binding.RET_OK),            # multiples of 16 below the tiles
+    (128, 128, 16, binding.RET_ERR_UNSUPPORTED),    # chunk outside {32, 64, 128}
+    (128, 128, 96, binding.RET_ERR_UNSUPPORTED),
+    (128, 128, 256, binding.RET_ERR_UNSUPPORTED),
+    (72, 128, 64, binding.RET_ERR_UNSUPPORTED),     # d_k not a multiple of 16
+    (8, 128, 64, binding.RET_ERR_UNSUPPORTED),
+    (272, 128, 64, binding.RET_ERR_UNSUPPORTED),    # d_k above 256
+    (128, 24, 64, binding.RET_ERR_UNSUPPORTED),     # d_v not a multiple of 16
+    (128, 1040, 64, binding.RET_ERR_UNSUPPORTED),   # d_v above 1024
+])
+def test_chunkwise_shape_support(lib, dk, dv, chunk, want):
+    """The bf16 chunkwise shapes: chunk 32, 64 or 128; d_k a multiple of 16 up
+    to 256; d_v a multiple of 16 up to 1024; anything else is refused on the
+    host with RET_ERR_UNSUPPORTED (checked through the host-only planning
+    calls, which share the chunkwise calls' shape rules)."""
+    size = ctypes.c_size_t(0)
+    n = ctypes.c_int(0)
+    assert lib.retention_chunkwise_workspace_size(2, 4, 1000, dk, dv, chunk, ctypes.byref(size)) == want
+    assert lib.retention_chunkwise_launches(2, 4, 1000, dk, dv, chunk, ctypes.byref(n)) == want
+    if want == binding.RET_OK:
+        assert n.value in (1, 2)
+
+
+def test_backward_launch_counts(lib):
+    """Kernels per bf16 gradient call: tensor-core widths gather, forward(s)
+    and place the results (plus the state kernels when states are given);
+    other widths take one CUDA-core launch."""
+    n = ctypes.c_int(0)
+    f = lib.retention_backward_launches
+    assert f(4, 8, 2048, 128, 128, 0, 0, 0, ctypes.byref(n)) == binding.RET_OK and n.value == 3
+    assert f(4, 8, 2048, 128, 128, 1, 1, 1, ctypes.byref(n)) == binding.RET_OK and n.value == 6
+    assert f(1, 16, 16384, 128, 256, 0, 0, 0, ctypes.byref(n)) == binding.RET_OK and n.value >= 4
+    assert f(1, 2, 100, 40, 24, 1, 1, 1, ctypes.byref(n)) == binding.RET_OK and n.value == 1
+    assert f(1, 2, 0, 128, 128, 0, 0, 1, ctypes.byref(n)) == binding.RET_OK and n.value == 1
+    assert f(0, 2, 10, 128, 128, 0, 0, 1, ctypes.byref(n)) == binding.RET_ERR_INVALID
+
+
 def test_f32_and_parallel_and_step_validation(lib):
     assert lib.retention_chunkwise_f32(P, P, P, P, P, None, 1, 1, 8, 32, 32, 0, None) == binding.RET_ERR_INVALID
     assert lib.retention_chunkwise_f32(P, P, P, P, P, None, 1, 1, 8, 32, 32, 129, None) == binding.RET_ERR_UNSUPPORTED

@@ -1,7 +1,9 @@
 """GPU parity of retention_backward (gradients of the forward with respect to
 q, k, v and the starting state) against the fp64 oracle's derivatives.
 
-Cases cover several internal chunks with a ragged last one, widths that are
+bf16 calls with d_k, d_v multiples of 16 up to 256 run on the tensor cores
+(each gradient a chunkwise forward of permuted operands); the others, and
+the fp32 twin, on the CUDA cores.  Cases cover several internal chunks with a ragged last one, widths that are
 not multiples of the 32-column slab, d_k != d_v, the widest rows (d_k 256,
 d_v 512), a starting state and a final-state gradient (each present or
 absent), decays 0, 0.5, 0.9 and 1, the fp32 twin, an empty sequence, and the
@@ -48,6 +50,9 @@ def _check(orc, q, k, v, g, dout, s0, ds, tol, f32=False, what=""):
     (1, 2, 130, 40, 24, True),      # slabs of 8 columns at the edge
     (1, 1, 100, 256, 512, True),    # widest rows
     (1, 2, 1, 128, 128, True),      # one token
+    (1, 2, 4500, 128, 256, True),   # tensor cores, d_k != d_v: two forward shapes, 128-token tiles, segments
+    (2, 2, 700, 256, 128, True),    # tensor cores, d_k = 256
+    (1, 3, 333, 48, 80, False),     # tensor cores, widths padded to the tiles
 ])
 def test_backward_matches_oracle(orc, B, H, N, dk, dv, states):
     q, k, v, dout, s0, ds = _case(B, H, N, dk, dv, 5, torch.bfloat16, states)

@@ -38,6 +38,13 @@ CASES = [
     (1, 2, 2048, 128, 128, 64),   # split into segments (pre-pass + combine)
     (1, 2, 4096, 128, 256, 128),  # segments with C=128 and two value tiles
     (1, 1, 3000, 256, 64, 128),   # segments, d_k = 256, ragged
+    # widths below the kernel's tiles (zero-padded by the loads) and chunk 32
+    (1, 2, 300, 64, 64, 64),      # d_k = 64: half of each 128-column Q/K box is padding
+    (2, 2, 333, 16, 16, 64),      # the narrowest widths
+    (1, 3, 250, 192, 96, 128),    # d_k = 192 on the 256 tiles; d_v = 96: second value tile half padding
+    (1, 2, 2100, 48, 208, 64),    # segments, d_v = 208 (four 64-wide tiles, the last one 16 wide)
+    (1, 2, 301, 128, 128, 32),    # chunk 32 (runs on 64-token tiles)
+    (1, 1, 2500, 80, 144, 32),    # chunk 32 with segments and padded widths
 ]
 
 
