@@ -25,12 +25,13 @@ Also reported on the same line:
   decode      the recurrent decode step on 64 sequences x 16 heads, d_k=128,
               d_v=256, fp32 state (128 MiB > L2): 1024 sequential steps
               captured in one CUDA graph; steps/s and HBM roofline.
-  groupnorm, rotate, mid_groupnorm_fused, mid_backward   the other kernels.
+  groupnorm, rotate, mid_groupnorm_fused, mid_backward, mid_parallel,
+  long_parallel   the other kernels.
 
 `--impl reference` times the fp64 CPU oracle alone on the same workload and
 metric (one batch row of the 7B-shaped workload per step, scaled to the
 batch) and prints its own line.
-`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b}`
+`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b,parallel,parallel_long}`
 runs one workload alone and prints its timing
 (used to give ncu a small, single-workload command).
 Under torchrun each rank runs its own replica (independent batches, no
@@ -451,19 +452,18 @@ def time_rotate(w, reps, dev, flush, seed=0):
     return times
 
 
-def backward_chunk(dk: int, dv: int) -> int:
-    """The chunk length the gradient kernel uses inside (32 for every width)."""
-    return 32
+def backward_chunk(w) -> int:
+    """The chunk length the gradient call's forwards use (128 from N = 4096 on)."""
+    return 128 if w["N"] >= 4096 else 64
 
 
-def backward_flops(w, C: int) -> int:
-    """Algorithmic flops of one gradient call at internal chunk C (causal part
-    only): per head-token the dq scan's scores, weighted rows, cross term and
-    state update, (C+1)(dk+dv) + 4 dk dv; the dk scan the same; the dv scan
-    its scores and rows, (C+1)(dk+dv), plus its cross term, 2 dk dv (the
-    state-gradient update is counted once, in the dk scan)."""
+def backward_flops(w) -> int:
+    """Algorithmic flops of one gradient call: three chunkwise forwards (dq,
+    and dk and dv walked from the last token), each (C+1)(dk+dv) + 4 dk dv per
+    head-token, causal part only."""
     B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
-    return B * H * N * (3 * (C + 1) * (dk + dv) + 10 * dk * dv)
+    C = backward_chunk(w)
+    return 3 * B * H * N * ((C + 1) * (dk + dv) + 4 * dk * dv)
 
 
 def backward_bytes(w) -> int:
@@ -474,8 +474,11 @@ def backward_bytes(w) -> int:
 
 
 def time_backward(w, reps, dev, flush, seed=0):
-    """ms per retention_backward call (no starting state, no final-state
-    gradient: the usual training case) on the workload, L2 flushed first."""
+    """Per-call device times (ms) of retention_backward (no starting state, no
+    final-state gradient: the usual training case), L2 flushed before each
+    call.  The call is captured once in a CUDA graph and replayed, so the
+    host-side work of its launches stays outside the timed region (eager calls
+    if capture is refused)."""
     from linear_attention_sequence_02_b300 import binding
     B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
     g = torch.Generator().manual_seed(seed)
@@ -483,27 +486,77 @@ def time_backward(w, reps, dev, flush, seed=0):
     gam = binding.gamma_schedule(H).to(dev)
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), None)
     stream = torch.cuda.current_stream(dev)
+
+    def call(s=None):
+        binding.retention_backward(q, k, v, gam, do, want_dstate_in=False, grads=grads, stream=s)
     for _ in range(3):
-        binding.retention_backward(q, k, v, gam, do, want_dstate_in=False, grads=grads)
+        call()
+    torch.cuda.synchronize(dev)
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call(torch.cuda.current_stream(dev))
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    except Exception:
+        graph = None
+        torch.cuda.synchronize(dev)
     times = []
     for _ in range(reps):
         flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        binding.retention_backward(q, k, v, gam, do, want_dstate_in=False, grads=grads)
+        if graph is not None:
+            graph.replay()
+        else:
+            call()
         b.record(stream)
         torch.cuda.synchronize(dev)
         times.append(a.elapsed_time(b))
     return times
 
 
-def oracle_sample(w, seed=0):
-    """One batch row of workload `w` (all H heads) as fp64 arrays for the oracle."""
+def parallel_flops(w) -> int:
+    """Algorithmic flops of the parallel form (causal part only): per head,
+    sum over n of (n+1) scores and (n+1) weighted value rows, N(N+1)(dk+dv)."""
+    B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
+    return B * H * N * (N + 1) * (dk + dv)
+
+
+def time_parallel(w, reps, dev, flush, seed=0):
+    """ms per retention_parallel call (tensor cores), L2 flushed before each call."""
     from linear_attention_sequence_02_b300 import binding, inputs
-    H, N, dk, dv = w["H"], w["N"], w["dk"], w["dv"]
-    q, k, v = inputs.qkv(1, H, N, dk, dv, seed, torch.bfloat16)
-    g = binding.gamma_schedule(H).double().numpy()
-    return tuple(x.double().numpy() for x in (q, k, v)) + (g,)
+    B, H, N, dk, dv = w["B"], w["H"], w["N"], w["dk"], w["dv"]
+    q, k, v = (x.to(dev) for x in inputs.qkv(B, H, N, dk, dv, seed, torch.bfloat16))
+    g = binding.gamma_schedule(H).to(dev)
+    out = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        binding.retention_parallel(q, k, v, g, out=out)
+    times = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.retention_parallel(q, k, v, g, out=out)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def parallel_entry(w, reps, dev, flush, tflops):
+    t = statistics.median(time_parallel(w, reps, dev, flush)) / 1e3
+    fl = parallel_flops(w)
+    return {"tokens_per_s": round(w["B"] * w["N"] / t, 1), "ms_per_call": round(t * 1e3, 5),
+            "config": {k: w[k] for k in ("B", "H", "N", "dk", "dv")} | {
+                "workload": f"{w['name']} retention parallel form (O(N^2), tensor cores)",
+                "l2": "flushed before each call (512 MiB write, then 512 MiB read)"},
+            "roofline": {"bound": "tensor", "achieved": round(fl / t / 1e12, 1), "peak": tflops, "unit": "TFLOP/s",
+                         "frac": round(fl / t / 1e12 / tflops, 4), "traffic": recorded_traffic(w["name"] + "_parallel"),
+                         "algorithmic_flops_per_call": fl},
+            "gpu_launches": 1}
 
 
 def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
@@ -630,24 +683,23 @@ def run_ours(args):
             "config": {"workload": "mid retention chunkwise fwd + GroupNorm over each head (fused epilogue)",
                        "out_layout": "[B, N, H, dv]"},
             "gpu_launches": nf}
-        # gradients of the mid workload
+        # the parallel form (tensor cores) on the mid and long workloads
+        extra["mid_parallel"] = parallel_entry(MID, 10, dev, flush, tflops)
+        extra["long_parallel"] = parallel_entry(LONG, 5, dev, flush, tflops)
+        # gradients of the mid workload (tensor cores: three chunkwise forwards)
         bt = statistics.median(time_backward(MID, 10, dev, flush)) / 1e3
-        props = torch.cuda.get_device_properties(dev)
-        max_mhz = clk.summary().get("sm_max_mhz") or 2032
-        fp32_peak = props.multi_processor_count * 128 * 2 * max_mhz * 1e6 / 1e12
-        bflops = backward_flops(MID, backward_chunk(MID["dk"], MID["dv"]))
+        bbytes = backward_bytes(MID)
         extra["mid_backward"] = {
             "tokens_per_s": round(MID["B"] * MID["N"] / bt, 1), "ms_per_call": round(bt * 1e3, 5),
             "config": {"workload": "mid retention gradients (dq, dk, dv), no states", "B": MID["B"], "H": MID["H"],
-                       "N": MID["N"], "dk": MID["dk"], "dv": MID["dv"],
-                       "internal_chunk": backward_chunk(MID["dk"], MID["dv"]),
-                       "l2": "flushed before each call (512 MiB write, then 512 MiB read)"},
-            "roofline": {"bound": "alu", "achieved": round(bflops / bt / 1e12, 2),
-                         "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
-                         "peak_kind": "fp32 FMA: SMs x 128 lanes x 2 flops x max SM clock",
-                         "frac": round(bflops / bt / 1e12 / fp32_peak, 4), "traffic": None,
-                         "hbm_frac": round(backward_bytes(MID) / bt / 1e9 / hbm, 4)},
-            "gpu_launches": 1}
+                       "N": MID["N"], "dk": MID["dk"], "dv": MID["dv"], "chunk": backward_chunk(MID),
+                       "l2": "flushed before each call (512 MiB write, then 512 MiB read)",
+                       "timing": "CUDA graph replay of the call"},
+            "roofline": {"bound": "hbm", "achieved": round(bbytes / bt / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(bbytes / bt / 1e9 / hbm, 4), "traffic": recorded_traffic("mid_backward"),
+                         "algorithmic_bytes_per_call": bbytes,
+                         "tensor_flops_frac": round(backward_flops(MID) / bt / 1e12 / tflops, 4)},
+            "gpu_launches": binding.backward_launches(MID["B"], MID["H"], MID["N"], MID["dk"], MID["dv"])}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -725,6 +777,12 @@ def run_only(args):
         print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps,
                           "tokens_per_s": round(wl["B"] * wl["N"] / (statistics.median(t) / 1e3), 1)}))
         return
+    if args.only in ("parallel", "parallel_long"):
+        wl = MID if args.only == "parallel" else LONG
+        t = time_parallel(wl, args.steps, dev, flush)
+        print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps,
+                          "tflops": round(parallel_flops(wl) / (statistics.median(t) / 1e3) / 1e12, 1)}))
+        return
     if args.only in ("groupnorm", "rotate"):
         fn, wl = (time_groupnorm, GROUPNORM) if args.only == "groupnorm" else (time_rotate, ROTATE)
         t = fn(wl, args.steps, dev, flush)
@@ -748,7 +806,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="with --only: batch rows instead of the workload's")
     ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate", "backward", "backward_long",
-                                       "backward_7b"], default=None)
+                                       "backward_7b", "parallel", "parallel_long"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -256,8 +256,15 @@ int retention_chunkwise_f32(const float *q, const float *k, const float *v, cons
 /*
  * retention_parallel / retention_parallel_f32 -- the parallel form
  * ("1. The Parallel Representation ..."): O = ((QK^T/sqrt(dk)) (.) D) V over
- * the whole sequence, no state.  Exported for correctness checks; tiled on
- * the CUDA cores.  dk, dv in [1, 256]; N >= 0.
+ * the whole sequence, no state; O(N^2) work, the training form of the pages.
+ * retention_parallel with dk a multiple of 16 in [16, 256] and dv a multiple
+ * of 16 in [16, 1024] runs on the tensor cores: per 128-row query tile a
+ * causal loop over 128-row key tiles, S = Q K_j^T and O += P~ V_j as
+ * tcgen05 MMAs (bf16 operands, fp32 accumulation in tensor memory), the decay
+ * gamma^(n-m) and 1/sqrt(dk) applied to S in registers; a key tile is skipped
+ * only where its largest decay factor is exactly zero in fp32.  Other widths
+ * (dk, dv in [1, 256]) and the float32 twin run tiled on the CUDA cores.
+ * N >= 0.
  */
 int retention_parallel(const void *q, const void *k, const void *v, const float *gamma,
                        void *out, int B, int H, int N, int dk, int dv, void *stream);

@@ -148,7 +148,7 @@ int backward_call(bool bf16, const void* q, const void* k, const void* v, const 
     return from_cuda(cudaMemcpyAsync(dstate_in, dstate, sizeof(float) * (size_t)B * H * dk * dv,
                                      cudaMemcpyDeviceToDevice, s));
   }
-  if (bf16 && ret::backward_tc_supported(dk, dv))
+  if (bf16 && ret::backward_tc_supported(dk, dv) && (int64_t)B * H <= 65535)
     return from_cuda(ret::launch_backward_tc(q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out, dstate_in, B,
                                              H, N, dk, dv, s));
   return from_cuda(ret::launch_backward(bf16, q, k, v, gamma, state_in, dout, dstate, dq, dk_out, dv_out,
@@ -184,7 +184,11 @@ int retention_gamma_schedule(int H, float* gamma_out) {
 
 int retention_device_status(unsigned int* flags, int clear) {
   if (!flags) return RET_ERR_INVALID;
-  return from_cuda(ret::read_device_status(flags, clear));
+  unsigned int a = 0, b = 0;
+  cudaError_t e = ret::read_device_status(&a, clear);  // synchronises the device first
+  if (e == cudaSuccess) e = ret::read_parallel_status(&b, clear);
+  *flags = a | b;
+  return from_cuda(e);
 }
 
 int retention_chunkwise_workspace_size(int B, int H, int N, int dk, int dv, int chunk,
@@ -297,6 +301,10 @@ int retention_parallel(const void* q, const void* k, const void* v, const float*
                        int B, int H, int N, int dk, int dv, void* stream) {
   int st = check_sequence(q, k, v, gamma, out, nullptr, B, H, N, dk, dv);
   if (st != RET_OK) return st;
+  if (ret::parallel_tc_supported(dk, dv)) {
+    if (N == 0) return RET_OK;
+    return from_cuda(ret::launch_parallel_tc(q, k, v, gamma, out, B, H, N, dk, dv, static_cast<cudaStream_t>(stream)));
+  }
   if (dk > 256 || dv > 256) return RET_ERR_UNSUPPORTED;
   if (N == 0) return RET_OK;
   if (B * H > 65535) return RET_ERR_UNSUPPORTED;
@@ -329,7 +337,7 @@ int retention_backward_launches(int B, int H, int N, int dk, int dv, int has_sta
     *launches = want_dstate_in ? 1 : 0;
     return RET_OK;
   }
-  if (!ret::backward_tc_supported(dk, dv)) {
+  if (!ret::backward_tc_supported(dk, dv) || (int64_t)B * H > 65535) {
     *launches = 1;
     return RET_OK;
   }

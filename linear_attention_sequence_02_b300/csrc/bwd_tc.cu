@@ -59,19 +59,33 @@ struct SeqJobs {
   int BH, N;
 };
 
-// grid.y = job; a grid-stride loop over 16-byte units of the job's tensor.
+// grid: (row blocks of one head, head, job).  A block copies kRowIters
+// groups of `rows` = 256 / w16 rows; thread t moves 16-byte unit t % w16 of
+// row t / w16 of each group, so every row is one contiguous run of a warp's
+// stores and every load is a whole row of the source.
+constexpr int kRowIters = 4;
 __global__ void __launch_bounds__(256) seq_gather_kernel(const __grid_constant__ SeqJobs J) {
-  const SeqJob j = J.job[blockIdx.y];
-  const uint32_t rows = (uint32_t)J.BH * (uint32_t)J.N;
-  const uint32_t units = rows * (uint32_t)j.w16;
-  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < units; u += gridDim.x * blockDim.x) {
-    const uint32_t row = u / (uint32_t)j.w16, c = u - row * (uint32_t)j.w16;
-    uint32_t srow = row;
-    if (j.reverse) {
-      const uint32_t bh = row / (uint32_t)J.N, n = row - bh * (uint32_t)J.N;
-      srow = bh * (uint32_t)J.N + ((uint32_t)J.N - 1u - n);
+  const SeqJob j = J.job[blockIdx.z];
+  const int w16 = j.w16;
+  const int rows = 256 / w16;  // rows per group
+  const int t = threadIdx.x;
+  const int r = t / w16, c = t - r * w16;
+  if (r >= rows) return;
+  const size_t head = (size_t)blockIdx.y * J.N;
+  const int n0 = blockIdx.x * rows * kRowIters + r;
+  uint4 x[kRowIters];
+#pragma unroll
+  for (int it = 0; it < kRowIters; ++it) {
+    const int n = n0 + it * rows;
+    if (n < J.N) {
+      const int sn = j.reverse ? J.N - 1 - n : n;
+      x[it] = __ldcs(j.src + (head + sn) * w16 + c);
     }
-    j.dst[u] = __ldcs(j.src + (size_t)srow * (uint32_t)j.w16 + c);
+  }
+#pragma unroll
+  for (int it = 0; it < kRowIters; ++it) {
+    const int n = n0 + it * rows;
+    if (n < J.N) __stcs(j.dst + (head + n) * w16 + c, x[it]);
   }
 }
 
@@ -160,10 +174,10 @@ int num_sms_current() {
 
 cudaError_t launch_seq(const SeqJobs& J, int n_jobs, cudaStream_t s) {
   if (n_jobs == 0) return cudaSuccess;
-  uint32_t most = 0;
-  for (int i = 0; i < n_jobs; ++i) most = std::max(most, (uint32_t)J.BH * (uint32_t)J.N * (uint32_t)J.job[i].w16);
-  const uint32_t blocks = std::min<uint32_t>((most + 255) / 256, 148u * 8u);
-  seq_gather_kernel<<<dim3(std::max(1u, blocks), n_jobs), 256, 0, s>>>(J);
+  int min_rows = 256;
+  for (int i = 0; i < n_jobs; ++i) min_rows = std::min(min_rows, 256 / J.job[i].w16);
+  const int blocks = (J.N + min_rows * kRowIters - 1) / (min_rows * kRowIters);
+  seq_gather_kernel<<<dim3(blocks, J.BH, n_jobs), 256, 0, s>>>(J);
   return cudaGetLastError();
 }
 
@@ -190,7 +204,7 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
   const int sms = num_sms_current();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int BH = B * H;
-  if ((uint64_t)BH * (uint64_t)N * 32ull >= (1ull << 31)) return cudaErrorNotSupported;  // 32-bit gather index
+  if (BH > 65535) return cudaErrorNotSupported;  // heads on the gather grid's y axis
   const float scale = (float)(1.0 / std::sqrt((double)dk));
   const int chunk = N >= 4096 ? 128 : 64;
   const bool same = dk == dv;

@@ -1172,6 +1172,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 // ---------------------------------------------------------------------------
 // host side
 
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1203,6 +1205,8 @@ bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows) 
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 // [B][N][H][dv] bf16 outputs (heads concatenated per token) viewed in 4-D as
 // (channel, head, token, batch row), boxes of 64 channels x 1 head x `rows`

@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/retention.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -29,6 +30,9 @@ cudaError_t launch_chunkwise_f32(const float* q, const float* k, const float* v,
                                  int N, int dk, int dv, int chunk, cudaStream_t s);
 
 // ---- tensor-core chunkwise (chunk_tc.cu) --------------------------------------
+// Tensor map of a [BH][N][d] bf16 tensor as 3-D (d, N, BH) with boxes of 64
+// columns x `rows` rows and 128-byte swizzle; boxes past the ends read zeros.
+bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows);
 struct ChunkPlan {
   int chunk;        // tokens per tile (64 or 128; a requested chunk of 32 runs as 64)
   int dk_tile;      // query/key columns the kernel is built for (128 or 256; dk <= dk_tile)
@@ -67,6 +71,13 @@ size_t backward_smem_bytes(int dk, int dv);
 cudaError_t launch_backward(bool bf16, const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, const void* dout, const float* dstate, void* dq, void* dk_out,
                             void* dv_out, float* dstate_in, int B, int H, int N, int dk, int dv, cudaStream_t s);
+
+// ---- parallel form on the tensor cores (parallel_tc.cu) ------------------------
+bool parallel_tc_supported(int dk, int dv);
+cudaError_t launch_parallel_tc(const void* q, const void* k, const void* v, const float* gamma, void* out, int B,
+                               int H, int N, int dk, int dv, cudaStream_t s);
+// Reads (and with `clear`, zeroes) the parallel kernels' device status word.
+cudaError_t read_parallel_status(unsigned int* flags, int clear);
 
 // ---- gradients of the forward on the tensor cores (bwd_tc.cu) -----------------
 // Widths the tensor-core gradients handle (each gradient is a chunkwise

@@ -92,14 +92,15 @@ def test_chunkwise_empty_sequence_zero_state():
 
 
 def test_chunkwise_unsupported_shapes_are_rejected():
-    q = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device=DEV)
+    """Widths that are not multiples of 16 and chunks outside {32, 64, 128}."""
+    q = torch.zeros(1, 1, 64, 72, dtype=torch.bfloat16, device=DEV)
     v = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(binding.RetentionError) as e:
         binding.retention_chunkwise(q, q, v, gammas(1).to(DEV), 64)
     assert e.value.status == binding.RET_ERR_UNSUPPORTED
     q = torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(binding.RetentionError) as e:
-        binding.retention_chunkwise(q, q, v, gammas(1).to(DEV), 32)
+        binding.retention_chunkwise(q, q, v, gammas(1).to(DEV), 16)
     assert e.value.status == binding.RET_ERR_UNSUPPORTED
 
 

@@ -70,3 +70,9 @@ def test_chunkwise_groupnorm_refuses_wide_heads():
     with pytest.raises(binding.RetentionError) as e:
         binding.retention_chunkwise_groupnorm(q, q, v, binding.gamma_schedule(1).to(DEV), 64)
     assert e.value.status == binding.RET_ERR_UNSUPPORTED
+    # a head's row must be a whole value tile without padding: d_v 64 or 128 only
+    for dv in (48, 96):
+        v = torch.zeros(1, 1, 64, dv, dtype=torch.bfloat16, device=DEV)
+        with pytest.raises(binding.RetentionError) as e:
+            binding.retention_chunkwise_groupnorm(q, q, v, binding.gamma_schedule(1).to(DEV), 64)
+        assert e.value.status == binding.RET_ERR_UNSUPPORTED
