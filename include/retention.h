@@ -354,6 +354,21 @@ int retention_gamma_schedule(int H, float *gamma_out);
  */
 int retention_device_status(unsigned int *flags, int clear);
 
+/*
+ * retention_test_stall_waits -- host function for tests of the failure path
+ * (no counterpart on the pages).  With `microseconds` > 0, every later
+ * launch of the tensor-core chunkwise kernel (retention_chunkwise and the
+ * calls built on it) makes one barrier wait that nothing completes, with
+ * that limit; the wait gives up, sets RET_DEV_WAIT_TIMEOUT in the device
+ * status word, and every role of the CTA unwinds exactly as after a real
+ * timeout (loads and MMAs in flight are waited for, tensor memory is
+ * released) and the kernel returns.  Outputs of such calls are undefined.
+ * 0 turns it off (the default).  The setting is process-wide and is read
+ * when a call enqueues its kernels.  microseconds above 10 000 000 return
+ * RET_ERR_INVALID.
+ */
+int retention_test_stall_waits(unsigned int microseconds);
+
 /* retention_status_string -- static text for a ret_status value. */
 const char *retention_status_string(int status);
 

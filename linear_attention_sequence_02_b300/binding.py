@@ -53,6 +53,7 @@ _SIGNATURES = {
     "retention_step_f32": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_gamma_schedule": [_i, _fp],
     "retention_device_status": [ctypes.POINTER(ctypes.c_uint), _i],
+    "retention_test_stall_waits": [ctypes.c_uint],
     "retention_status_string": [_i],
     "retention_version": [],
 }
@@ -115,6 +116,12 @@ def gamma_schedule(H: int) -> torch.Tensor:
     out = (ctypes.c_float * H)()
     _check("retention_gamma_schedule", lib().retention_gamma_schedule(H, out))
     return torch.tensor(list(out), dtype=torch.float32)
+
+
+def test_stall_waits(microseconds: int) -> None:
+    """Failure-path test setting: > 0 makes every later chunkwise launch give
+    up one wait after `microseconds` (see retention_test_stall_waits); 0 off."""
+    _check("retention_test_stall_waits", lib().retention_test_stall_waits(int(microseconds)))
 
 
 def device_status(clear: bool = True) -> int:

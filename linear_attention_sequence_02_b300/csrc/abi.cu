@@ -182,6 +182,12 @@ int retention_gamma_schedule(int H, float* gamma_out) {
   return RET_OK;
 }
 
+int retention_test_stall_waits(unsigned int microseconds) {
+  if (microseconds > 10000000u) return RET_ERR_INVALID;  // at most 10 s
+  ret::g_test_stall_us.store(microseconds, std::memory_order_relaxed);
+  return RET_OK;
+}
+
 int retention_device_status(unsigned int* flags, int clear) {
   if (!flags) return RET_ERR_INVALID;
   unsigned int a = 0, b = 0;
@@ -208,7 +214,7 @@ int retention_chunkwise_launches(int B, int H, int N, int dk, int dv, int chunk,
   const int sms = num_sms();
   int st = plan_chunkwise(B, H, N, dk, dv, chunk, sms > 0 ? sms : 148, &plan);
   if (st != RET_OK) return st;
-  *launches = N == 0 ? 0 : plan.launches;
+  *launches = N == 0 ? 0 : ret::chunk_tc_launch_count(plan);
   return RET_OK;
 }
 

@@ -356,7 +356,7 @@ int backward_tc_launches(int B, int H, int N, int dk, int dv, bool has_state_in,
     ChunkPlan plan;
     const int parts = dk == dv ? 3 : (gi == 0 ? 2 : 1);
     if (!chunk_tc_plan(parts * B, H, N, gi == 0 ? dv : dk, gi == 0 ? dk : dv, chunk, sms, &plan)) return -1;
-    n += plan.launches;
+    n += chunk_tc_launch_count(plan);
   }
   return n;
 }

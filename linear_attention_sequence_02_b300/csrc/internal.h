@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -46,6 +47,9 @@ struct ChunkPlan {
 };
 // Fills `plan` for a supported shape; returns false for unsupported shapes.
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan);
+// Kernels a call with this plan enqueues on the current device: 1, or 2 where
+// a split sequence cannot run as clusters (pre-pass, then main pass).
+int chunk_tc_launch_count(const ChunkPlan& plan);
 // GroupNorm of the outputs fused into the chunkwise epilogue (one value tile
 // per head): weight, bias [H dv] (nullable: one, zero) and eps; the outputs are
 // then written [B][N][H][dv].
@@ -62,6 +66,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             int N, int dk, int dv, const ChunkPlan& plan, float* workspace,
                             const ChunkNorm* norm, float scale, cudaStream_t s);
 cudaError_t read_device_status(unsigned int* flags, int clear);
+// Failure-path test setting read by every chunkwise launch (0: off).
+extern std::atomic<unsigned int> g_test_stall_us;
 
 // ---- gradients of the forward on the CUDA cores (backward.cu) ------------------
 // The chunk length the kernel uses inside and its dynamic shared memory for
