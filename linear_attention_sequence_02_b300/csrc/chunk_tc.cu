@@ -1430,11 +1430,17 @@ cudaError_t launch_fused(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // The shared-memory opt-in is a per-device attribute of each kernel variant.
+  static std::atomic<unsigned long long> configured{0};
+  const unsigned long long bit = 1ull << dev;
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
   std::atomic<unsigned char>* fits = &g_cluster_fits[dev][p.segments];
   unsigned char f = fits->load(std::memory_order_acquire);
   if (f == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
     if (e != cudaSuccess) {
