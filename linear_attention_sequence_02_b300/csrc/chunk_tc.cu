@@ -1488,10 +1488,6 @@ int chunk_tc_launch_count(const ChunkPlan& plan) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 1;
   // not asked yet: ask with the variant the plan selects, without launching
   if (g_cluster_fits[dev][plan.segments].load(std::memory_order_acquire) == 0) {
-    TcParams p = {};
-    p.segments = plan.segments;
-    p.BH = 1;
-    p.n_dv_tiles = 1;
     using K = decltype(&chunk_tc_fused_kernel<64, 128, 128, false>);
     K kern = chunk_tc_fused_kernel<64, 128, 128, false>;
     cudaLaunchConfig_t cfg = {};
