@@ -40,8 +40,9 @@ def test_noalloc_matches_allocating_entry_point_on_two_calls():
 
 
 def test_noalloc_rejects_plans_beyond_static_scratch():
-    # One long head with d_k = 256 splits into ~143 segments: ~9.3 MB of states.
-    B, H, N, dk, dv, C = 1, 1, 128000, 256, 64, 128
+    # Nine wide heads (d_k 256, d_v 1024: 72 value tiles) split into two
+    # segments: 9 x 256 x 1024 float32 states, 9.4 MB, beyond the 8 MiB array.
+    B, H, N, dk, dv, C = 1, 9, 2048, 256, 1024, 128
     assert binding.chunkwise_workspace_size(B, H, N, dk, dv, C) > STATIC_SCRATCH_BYTES
     q = torch.empty(B, H, N, dk, dtype=torch.bfloat16, device=DEV)
     v = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=DEV)
