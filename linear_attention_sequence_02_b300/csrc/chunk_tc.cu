@@ -96,9 +96,7 @@ __device__ __forceinline__ int acc_row(int M, int quarter, int lane) {
   return lane < 16 ? 16 * quarter + lane : -1;
 }
 
-// BUDGET: shared memory the layout may use (all of it, or, for the state-only
-// pass inside the one-launch kernel, what lies below the main layout's tables).
-template <int C, int DK, int DVT, bool SO, int BUDGET = kMaxSmemPerBlock>
+template <int C, int DK, int DVT, bool SO>
 struct Cfg {
   static_assert(C == 64 || C == 128, "chunk");
   static_assert(DK == 128 || DK == 256, "dk");
@@ -121,22 +119,22 @@ struct Cfg {
   // so that neither V slots nor snapshots wait for output stores; else its own
   // staging buffer and one snapshot buffer; else (no room) the output tile is
   // staged in the chunk's V slot.
-  static constexpr bool kSepStage = !SO && bytes(kMinQK, 3, 1, 1) <= BUDGET;
-  static constexpr int NSB = !SO && kSepStage && bytes(kMinQK, 3, 2, 1) <= BUDGET ? 2 : 1;
+  static constexpr bool kSepStage = !SO && bytes(kMinQK, 3, 1, 1) <= kMaxSmemPerBlock;
+  static constexpr int NSB = !SO && kSepStage && bytes(kMinQK, 3, 2, 1) <= kMaxSmemPerBlock ? 2 : 1;
   static constexpr int NSTG = kSepStage ? 1 : 0;
   static constexpr int pick_nqk() {
     int n = 6;
-    while (n > H && bytes(n, n, NSB, NSTG) > BUDGET) --n;
+    while (n > H && bytes(n, n, NSB, NSTG) > kMaxSmemPerBlock) --n;
     return n;
   }
   static constexpr int NQK = pick_nqk();
   static constexpr int pick_nv() {
     int v = NQK;
-    while (!(SO && H == 1) && v < 8 && bytes(NQK, v + 1, NSB, NSTG) <= BUDGET) ++v;
+    while (!(SO && H == 1) && v < 8 && bytes(NQK, v + 1, NSB, NSTG) <= kMaxSmemPerBlock) ++v;
     return v;
   }
   static constexpr int NV = pick_nv();
-  static_assert(NQK >= H && bytes(NQK, NV, NSB, NSTG) <= BUDGET, "shared memory");
+  static_assert(NQK >= H && bytes(NQK, NV, NSB, NSTG) <= kMaxSmemPerBlock, "shared memory");
   static constexpr int oV = NQK * kQK;
   static constexpr int oSb = oV + NV * kV;
   static constexpr int oStg = oSb + NSB * kSb;
@@ -192,23 +190,15 @@ struct TcParams {
   int dk;            // query/key width (<= DK; the columns past it are zero-filled by the loads)
   float scale;       // factor of the query (1/sqrt(dk) unless the caller sets another)
   unsigned int test_stall_us;  // > 0: failure-path test (see retention_test_stall_waits)
-  int fused;         // 1: one launch, the segments of a (head, value tile) as one cluster
 };
 
-// Position of this CTA: value tile, head (b*H+h) and sequence segment.  The
-// two-launch plan orders CTAs value tile fastest, then head, then segment; the
-// one-launch plan puts the segments of one (head, value tile) next to each
-// other, so that they form one thread-block cluster.
+// Position of this CTA: value tile, head (b*H+h) and sequence segment, value
+// tile fastest, then head, then segment.
 struct CtaPos {
   int dvt, bh, seg;
 };
 __device__ __forceinline__ CtaPos cta_pos(const TcParams& p) {
   int idx = blockIdx.x;
-  if (p.fused) {
-    const int seg = idx % p.segments;
-    idx /= p.segments;
-    return CtaPos{idx % p.n_dv_tiles, idx / p.n_dv_tiles, seg};
-  }
   const int dvt = idx % p.n_dv_tiles;
   idx /= p.n_dv_tiles;
   return CtaPos{dvt, idx % p.BH, idx / p.BH};
@@ -365,9 +355,9 @@ __device__ __forceinline__ void scale_rows_bf16(uint8_t* base, int tid, F f) {
 // global stores are coalesced.  Kept out of line: everything it needs is
 // recomputed from the launch parameters, so no register stays live across the
 // roles for it.
-template <int C, int DK, int DVT, bool SO, int BUDGET = kMaxSmemPerBlock>
+template <int C, int DK, int DVT, bool SO>
 __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, uint32_t tmem) {
-  using L = Cfg<C, DK, DVT, SO, BUDGET>;
+  using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H;
   const CtaPos pos = cta_pos(p);
   const int dvt = pos.dvt, bh = pos.bh, seg = pos.seg;
@@ -430,9 +420,9 @@ struct RoleCtx {
 // The four roles of a CTA (producer, MMA issuer, state group, output group).
 // FAST selects the rescaled form; a CTA picks one instantiation at its start,
 // so the code it runs holds no branches of the other form.
-template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM, int BUDGET = kMaxSmemPerBlock>
+template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM>
 __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x) {
-  using L = Cfg<C, DK, DVT, SO, BUDGET>;
+  using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
   constexpr bool fast = FAST;
   constexpr bool look = L::kLookahead;
@@ -1103,9 +1093,9 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
 }
 
 // Initialises the barriers of layout Cfg<C, DK, DVT, SO> (one thread).
-template <int C, int DK, int DVT, bool SO, int BUDGET = kMaxSmemPerBlock>
+template <int C, int DK, int DVT, bool SO>
 __device__ __forceinline__ void init_barriers(uint32_t sbase) {
-  using L = Cfg<C, DK, DVT, SO, BUDGET>;
+  using L = Cfg<C, DK, DVT, SO>;
   auto bar = [&](int i) { return sbase + L::oBar + 8 * i; };
   for (int i = 0; i < L::NQK; ++i) {
     mbar_init(bar(L::bQkFull + i), 1);
@@ -1136,14 +1126,6 @@ __device__ __forceinline__ void init_barriers(uint32_t sbase) {
   mbar_init(bar(L::bFin), SO ? 1 : 2);
   for (int i = 0; i < L::NV; ++i) mbar_init(bar(L::bSDone + i), 1);
   mbar_init(bar(L::bNever), 1);  // nothing ever arrives here (failure-path test)
-}
-
-// Invalidates the barriers of layout Cfg<C, DK, DVT, SO> (one thread), before
-// their shared memory is handed to another use.
-template <int C, int DK, int DVT, bool SO, int BUDGET = kMaxSmemPerBlock>
-__device__ __forceinline__ void inval_barriers(uint32_t sbase) {
-  using L = Cfg<C, DK, DVT, SO, BUDGET>;
-  for (int i = 0; i < L::kBars; ++i) mbar_inval(sbase + L::oBar + 8 * i);
 }
 
 template <int C, int DK, int DVT, bool SO, bool NORM>
@@ -1201,109 +1183,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   write_final_state<C, DK, DVT, SO>(p, sm, tmem);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem, L::kTmemCols);
-  }
-}
-
-// One launch for a sequence cut into segments.  The segments of one (head,
-// value tile) are one thread-block cluster.  Every CTA but the last segment's
-// first runs the state-only pass over its own segment (the roles of the
-// pre-pass, in the state-only shared-memory layout, which lies below the main
-// layout's tables and barriers) and writes its local end state to the
-// workspace; a cluster barrier with release/acquire order makes those states
-// visible to the whole cluster; then every CTA sums its predecessors' states
-// into its initial state and runs the main pass.  The cluster barrier needs
-// no flags in memory, and the cluster's CTAs are resident together, so no
-// CTA waits for one that has not started.
-template <int C, int DK, int DVT, bool NORM>
-__global__ void __launch_bounds__(kThreads, 1)
-chunk_tc_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
-                      const TcParams p) {
-  using L = Cfg<C, DK, DVT, false>;
-  constexpr int BS = L::oPw;  // the state-only pass may use everything below the main layout's tables
-  using LS = Cfg<C, DK, DVT, true, BS>;
-  static_assert(LS::oCState + 4 <= L::oPw, "the state-only layout must end below the main pass's tables");
-  static_assert(LS::kTmemCols <= L::kTmemCols, "tmem");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const uint32_t sbase = smem_u32(sm);
-  float* pw = reinterpret_cast<float*>(sm + L::oPw);
-  float* pw_s = reinterpret_cast<float*>(sm + LS::oPw);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oAbort);
-  volatile int* abort_s = reinterpret_cast<volatile int*>(sm + LS::oAbort);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oSlot);
-  const CtaPos pos = cta_pos(p);
-  const bool state_pass = pos.seg < p.segments - 1;
-  const int head = pos.bh % p.H;
-  const float g = p.gamma[head];
-  const float lg = g > 0.f ? log2f(g) : 0.f;
-  const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
-  const int warp = threadIdx.x >> 5;
-
-  // ---- set-up of both passes ----
-  if (threadIdx.x == 0) {
-    init_barriers<C, DK, DVT, false>(sbase);
-    *abort_flag = 0;
-    if (state_pass) {
-      init_barriers<C, DK, DVT, true, BS>(sbase);
-      *abort_s = 0;
-    }
-    fence_mbar_init();
-    prefetch_tensormap(&tmq);
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-    prefetch_tensormap(&tmo);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
-    tmem_relinquish();
-  }
-  for (int d = threadIdx.x; d <= C; d += kThreads) {
-    const float x = gamma_pow(g, lg, (float)d);
-    pw[d] = x;
-    if (state_pass) pw_s[d] = x;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const float inv_gC = fast ? 1.f / pw[C] : 1.f;
-  const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC};
-
-  // ---- state-only pass over this segment: its local end state ----
-  if (state_pass) {
-    if (fast) chunk_roles<C, DK, DVT, true, true, false, BS>(p, x);
-    else chunk_roles<C, DK, DVT, true, false, false, BS>(p, x);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    write_final_state<C, DK, DVT, true, BS>(p, sm, tmem);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      inval_barriers<C, DK, DVT, true, BS>(sbase);  // their memory becomes ring space
-      if (*abort_s) *abort_flag = 1;            // a timed-out state pass ends the main pass too
-    }
-  }
-  // ---- the cluster's local end states are written and visible ----
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_release_acquire();
-  tc_fence_after();
-
-  // ---- main pass ----
-  if (fast) chunk_roles<C, DK, DVT, false, true, NORM>(p, x);
-  else chunk_roles<C, DK, DVT, false, false, NORM>(p, x);
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  write_final_state<C, DK, DVT, false>(p, sm, tmem);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1401,75 +1280,13 @@ cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return cudaGetLastError();
 }
 
-// Per device and cluster size (2..8): 0 not asked yet, 1 clusters of one
-// CTA per SM (every variant's shared memory fills an SM) can be resident, 2 not.
-std::atomic<unsigned char> g_cluster_fits[64][9];
-
-// One launch with the segments of each (head, value tile) as a cluster; false
-// (and nothing launched) when clusters of that size with this kernel's
-// shared memory cannot be resident on the device.
-template <int C, int DK, int DVT, bool NORM>
-cudaError_t launch_fused(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mo, const TcParams& p, bool* launched, cudaStream_t s) {
-  using L = Cfg<C, DK, DVT, false>;
-  auto kern = chunk_tc_fused_kernel<C, DK, DVT, NORM>;
-  *launched = false;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 64 || p.segments < 2 || p.segments > 8) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.BH * p.n_dv_tiles * p.segments));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::kAlloc;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.segments;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // The shared-memory opt-in is a per-device attribute of each kernel variant.
-  static std::atomic<unsigned long long> configured{0};
-  const unsigned long long bit = 1ull << dev;
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_release);
-  }
-  std::atomic<unsigned char>* fits = &g_cluster_fits[dev][p.segments];
-  unsigned char f = fits->load(std::memory_order_acquire);
-  if (f == 0) {
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();  // a refused query leaves no error behind: fall back
-      clusters = 0;
-    }
-    f = clusters >= 1 ? 1 : 2;
-    fits->store(f, std::memory_order_release);
-  }
-  if (f != 1) return cudaSuccess;
-  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, p);
-  if (e != cudaSuccess) return e;
-  *launched = true;
-  return cudaGetLastError();
-}
-
 template <int C, int DK, int DVT, bool NORM>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        const CUtensorMap& mo, TcParams p, cudaStream_t s) {
+                        const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   const bool split = p.segments > 1;
   if (split) {
-    // preferred: one launch, segments as clusters
-    p.fused = 1;
-    bool launched = false;
-    cudaError_t e = launch_fused<C, DK, DVT, NORM>(mq, mk, mv, mo, p, &launched, s);
-    if (e != cudaSuccess || launched) return e;
-    p.fused = 0;
-    // else the state-only pre-pass, then the main pass with programmatic dependent launch
-    e = launch_one<C, DK, DVT, true, false>(mq, mk, mv, mo, p, p.BH * (p.segments - 1) * p.n_dv_tiles, false, s);
+    cudaError_t e = launch_one<C, DK, DVT, true, false>(mq, mk, mv, mo, p, p.BH * (p.segments - 1) * p.n_dv_tiles,
+                                                        false, s);
     if (e != cudaSuccess) return e;
   }
   return launch_one<C, DK, DVT, false, NORM>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
@@ -1482,35 +1299,7 @@ int pick_dvt(int dv) { return dv % 128 == 0 ? 128 : 64; }
 
 std::atomic<unsigned int> g_test_stall_us{0};
 
-int chunk_tc_launch_count(const ChunkPlan& plan) {
-  if (plan.segments <= 1) return 1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 1;
-  // not asked yet: ask with the variant the plan selects, without launching
-  if (g_cluster_fits[dev][plan.segments].load(std::memory_order_acquire) == 0) {
-    using K = decltype(&chunk_tc_fused_kernel<64, 128, 128, false>);
-    K kern = chunk_tc_fused_kernel<64, 128, 128, false>;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.segments);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<64, 128, 128, false>::kAlloc;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)plan.segments;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.dynamicSmemBytes) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return 1;  // no device to ask: the clustered launch is the plan
-    }
-    g_cluster_fits[dev][plan.segments].store(clusters >= 1 ? 1 : 2, std::memory_order_release);
-  }
-  return g_cluster_fits[dev][plan.segments].load(std::memory_order_acquire) == 1 ? 1 : 2;
-}
+int chunk_tc_launch_count(const ChunkPlan& plan) { return plan.launches; }
 
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan) {
   // chunk 32 runs on 64-token tiles: the chunk length is a tiling choice that
@@ -1532,7 +1321,6 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   int segs = 1;
   if (num_sms > 0 && units < num_sms) segs = (int)(num_sms / units);
   segs = std::max(1, std::min(segs, plan->n_chunks / 4));
-  segs = std::min(segs, 8);  // the segments of one (head, value tile) form one cluster of at most 8
   int seg_chunks = plan->n_chunks > 0 ? (plan->n_chunks + segs - 1) / segs : 1;
   if (plan->n_chunks > 0) segs = (plan->n_chunks + seg_chunks - 1) / seg_chunks;  // no empty segment
   plan->segments = std::max(1, segs);
@@ -1541,7 +1329,7 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   plan->workspace_bytes = plan->segments > 1 ? sizeof(float) * (size_t)B * H * (plan->segments - 1) *
                                                    plan->dk_tile * (size_t)plan->n_dv_tiles * dvt
                                              : 0;
-  plan->launches = 1;  // segments: one clustered launch (two launches only where clusters cannot be resident)
+  plan->launches = plan->segments > 1 ? 2 : 1;
   if ((long long)units * plan->segments > INT32_MAX) return false;
   return true;
 }
@@ -1578,7 +1366,6 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.n_chunks = plan.n_chunks;
   p.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)dk));
   p.test_stall_us = g_test_stall_us.load(std::memory_order_relaxed);
-  p.fused = 0;
   const bool t128 = plan.dvt == 128;
   const int dkt = plan.dk_tile;
   if (norm) {

@@ -47,8 +47,8 @@ struct ChunkPlan {
 };
 // Fills `plan` for a supported shape; returns false for unsupported shapes.
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan);
-// Kernels a call with this plan enqueues on the current device: 1, or 2 where
-// a split sequence cannot run as clusters (pre-pass, then main pass).
+// Kernels a call with this plan enqueues (2 when the sequence is split:
+// state-only pre-pass, then main pass).
 int chunk_tc_launch_count(const ChunkPlan& plan);
 // GroupNorm of the outputs fused into the chunkwise epilogue (one value tile
 // per head): weight, bias [H dv] (nullable: one, zero) and eps; the outputs are

@@ -36,10 +36,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                "r"(bytes)
                : "memory");
 }
-// Invalidates a barrier object before its shared memory is used for anything else.
-__device__ __forceinline__ void mbar_inval(uint32_t bar) {
-  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 // Wait for phase `parity`, suspending the thread in hardware until the phase
 // completes or at most 1 ms has passed (the suspend-time hint): true once the
 // phase has completed.  The thread takes no issue slots while suspended.
@@ -120,14 +116,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // Wait until the preceding grid has completed and its memory is visible
 // (returns at once when the launch had no such dependency).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// ---- thread-block clusters -------------------------------------------------------
-// Barrier over every thread of every CTA in the cluster: memory operations
-// before it (global and shared) are visible, at cluster scope, to every thread
-// of the cluster after it.  Every thread must execute it, warp-converged.
-__device__ __forceinline__ void cluster_sync_release_acquire() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 // ---- named barriers -----------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
