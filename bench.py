@@ -25,13 +25,13 @@ Also reported on the same line:
   decode      the recurrent decode step on 64 sequences x 16 heads, d_k=128,
               d_v=256, fp32 state (128 MiB > L2): 1024 sequential steps
               captured in one CUDA graph; steps/s and HBM roofline.
-  groupnorm, rotate, mid_groupnorm_fused, mid_backward, mid_parallel,
-  long_parallel   the other kernels.
+  groupnorm, rotate, mid_groupnorm_fused, mid_rotated, mid_backward,
+  mid_parallel, long_parallel   the other kernels.
 
 `--impl reference` times the fp64 CPU oracle alone on the same workload and
 metric (one batch row of the 7B-shaped workload per step, scaled to the
 batch) and prints its own line.
-`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b,parallel,parallel_long}`
+`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b,parallel,parallel_long,rotated}`
 runs one workload alone and prints its timing
 (used to give ncu a small, single-workload command).
 Under torchrun each rank runs its own replica (independent batches, no
@@ -517,6 +517,52 @@ def time_backward(w, reps, dev, flush, seed=0):
     return times
 
 
+def time_rotated(w, reps, dev, flush, seed=0):
+    """ms per call of the chunkwise forward of rotated q and k: the fused call
+    (retention_chunkwise_rotated) and the separate path (retention_rotate on
+    q, on k, then retention_chunkwise), each captured in a CUDA graph and
+    replayed with L2 flushed before each call."""
+    from linear_attention_sequence_02_b300 import binding, inputs
+    B, H, N, dk, dv, C = w["B"], w["H"], w["N"], w["dk"], w["dv"], w["chunk"]
+    q, k, v = (x.to(dev) for x in inputs.qkv(B, H, N, dk, dv, seed, torch.bfloat16))
+    g = binding.gamma_schedule(H).to(dev)
+    th = torch.tensor([10000.0 ** (-2.0 * j / dk) for j in range(dk // 2)], dtype=torch.float32, device=dev)
+    out = torch.empty(B, H, N, dv, dtype=torch.bfloat16, device=dev)
+    st = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    rq, rk = torch.empty_like(q), torch.empty_like(k)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused(s=None):
+        binding.retention_chunkwise_rotated(q, k, v, g, th, 0, C, out=out, state_out=st, stream=s)
+
+    def separate(s=None):
+        binding.retention_rotate(q, th, 0, out=rq, stream=s)
+        binding.retention_rotate(k, th, 0, out=rk, stream=s)
+        binding.retention_chunkwise(rq, rk, v, g, C, out=out, state_out=st, stream=s)
+    res = {}
+    for name, fn in (("fused", fused), ("separate", separate)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn(torch.cuda.current_stream(dev))
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(reps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+        del graph
+    return res
+
+
 def parallel_flops(w) -> int:
     """Algorithmic flops of the parallel form (causal part only): per head,
     sum over n of (n+1) scores and (n+1) weighted value rows, N(N+1)(dk+dv)."""
@@ -683,6 +729,16 @@ def run_ours(args):
             "config": {"workload": "mid retention chunkwise fwd + GroupNorm over each head (fused epilogue)",
                        "out_layout": "[B, N, H, dv]"},
             "gpu_launches": nf}
+        # the chunkwise forward of rotated q and k: rotation fused, against separate passes
+        rr = time_rotated(MID, args.steps, dev, flush)
+        extra["mid_rotated"] = {
+            "tokens_per_s": round(MID["B"] * MID["N"] / (rr["fused"] / 1e3), 1), "ms_per_call": round(rr["fused"], 5),
+            "separate_ms": round(rr["separate"], 5),
+            "config": {"workload": "mid retention chunkwise fwd of rotated q, k (rotation fused in the kernels)",
+                       "separate": "retention_rotate on q and on k, then retention_chunkwise",
+                       "timing": "CUDA graph replay, L2 flushed before each call"},
+            "gpu_launches": binding.chunkwise_launches(MID["B"], MID["H"], MID["N"], MID["dk"], MID["dv"],
+                                                       MID["chunk"])}
         # the parallel form (tensor cores) on the mid and long workloads
         extra["mid_parallel"] = parallel_entry(MID, 10, dev, flush, tflops)
         extra["long_parallel"] = parallel_entry(LONG, 5, dev, flush, tflops)
@@ -777,6 +833,10 @@ def run_only(args):
         print(json.dumps({"only": args.only, "ms_per_call": statistics.median(t), "launches": args.steps,
                           "tokens_per_s": round(wl["B"] * wl["N"] / (statistics.median(t) / 1e3), 1)}))
         return
+    if args.only == "rotated":
+        r = time_rotated(MID, args.steps, dev, flush)
+        print(json.dumps({"only": "rotated", "fused_ms": r["fused"], "separate_ms": r["separate"]}))
+        return
     if args.only in ("parallel", "parallel_long"):
         wl = MID if args.only == "parallel" else LONG
         t = time_parallel(wl, args.steps, dev, flush)
@@ -806,7 +866,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="with --only: batch rows instead of the workload's")
     ap.add_argument("--only", choices=["mid", "long", "7b", "decode", "groupnorm", "rotate", "backward", "backward_long",
-                                       "backward_7b", "parallel", "parallel_long"], default=None)
+                                       "backward_7b", "parallel", "parallel_long", "rotated"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -122,6 +122,30 @@ int retention_chunkwise_from_state(const void *q, const void *k, const void *v, 
                                    int B, int H, int N, int dk, int dv, int chunk, void *stream);
 
 /*
+ * retention_chunkwise_rotated -- retention_chunkwise_from_state of the queries
+ * and keys turned by the position phase rotation of "2. Relative Position via
+ * Complex Exponential Phase Rotations" (as retention_rotate below, with the
+ * same theta and n0 for q and k), the rotation fused into the kernels' load
+ * stage: each Q/K tile is turned in shared memory after it lands and before
+ * the tensor cores read it, so q and k are read from HBM once and the turned
+ * copies are never written:
+ *
+ *   out = chunkwise(rotate(q, theta, n0), rotate(k, theta, n0), v, gamma; state_in)
+ *
+ * The turned pairs are rounded to bf16 (as retention_rotate's output would
+ * be).  theta: float32 [dk/2] device memory, 4-byte aligned; n0 >= 0 the
+ * position of token 0; state_in nullable as for
+ * retention_chunkwise_from_state (it must not equal state_out).  Shapes and
+ * the workspace as for retention_chunkwise; n0 plus N rounded up to the tile
+ * length (64, or 128 for chunk 128) must not exceed 2^24 (positions exact in
+ * float32), else RET_ERR_UNSUPPORTED.
+ */
+int retention_chunkwise_rotated(const void *q, const void *k, const void *v, const float *gamma,
+                                const float *theta, int n0, const float *state_in, void *out,
+                                float *state_out, int B, int H, int N, int dk, int dv, int chunk,
+                                void *stream);
+
+/*
  * retention_rotate -- the position phase rotation of queries or keys: "2.
  * Relative Position via Complex Exponential Phase Rotations" multiplies the
  * query and key of token n by e^(i n theta), so that their product depends on
@@ -284,6 +308,17 @@ int retention_step(const void *q, const void *k, const void *v, float *state, vo
                    int B, int H, int dk, int dv, void *stream);
 int retention_step_f32(const float *q, const float *k, const float *v, float *state, float *out,
                        int B, int H, int dk, int dv, void *stream);
+
+/*
+ * retention_step_rotated -- retention_step for the token at position `pos`,
+ * with q and k turned by the position phase rotation (theta float32 [dk/2],
+ * as retention_rotate) as they are loaded, in float32, before the state
+ * update: the decode step that continues a sequence prefilled by
+ * retention_chunkwise_rotated (pos = the number of tokens before it, n0
+ * included).  0 <= pos < 2^24 and dk even, else RET_ERR_UNSUPPORTED.
+ */
+int retention_step_rotated(const void *q, const void *k, const void *v, const float *theta, int pos,
+                           float *state, void *out, int B, int H, int dk, int dv, void *stream);
 
 /*
  * retention_backward -- gradients of the forward (any of its forms: they

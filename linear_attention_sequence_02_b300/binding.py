@@ -34,6 +34,8 @@ _fp = ctypes.POINTER(ctypes.c_float)
 _SIGNATURES = {
     "retention_chunkwise": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_chunkwise_from_state": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+    "retention_chunkwise_rotated": [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+    "retention_step_rotated": [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp],
     "retention_chunkwise_groupnorm": [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _i, _i, _i, _i, _i,
                                       _i, _vp],
     "retention_chunkwise_ws": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
@@ -179,6 +181,23 @@ def retention_chunkwise_from_state(q, k, v, gamma, chunk: int, state_in, out=Non
     args = args[:4] + [_p(state_in)] + args[4:]
     _check("retention_chunkwise_from_state",
            lib().retention_chunkwise_from_state(*args, _stream(stream)))
+    return out, state_out
+
+
+def retention_chunkwise_rotated(q, k, v, gamma, theta, n0: int, chunk: int, state_in=None, out=None,
+                                state_out=None, want_state: bool = True, stream=None):
+    """bf16 chunkwise forward of q and k turned by the position phase rotation
+    (theta float32 [dk/2], token 0 at position n0), the rotation fused into
+    the kernels; optional starting state.  Returns (out, state_out or None)."""
+    args, out, state_out = _sequence_call("retention_chunkwise", torch.bfloat16, q, k, v, gamma,
+                                          out, state_out, want_state, [int(chunk)], stream)
+    B, H, N, dk, dv = _seq_dims(q, v)
+    _need(theta, "theta", torch.float32, (dk // 2,))
+    if state_in is not None:
+        _need(state_in, "state_in", torch.float32, (B, H, dk, dv))
+    _check("retention_chunkwise_rotated",
+           lib().retention_chunkwise_rotated(_p(q), _p(k), _p(v), _p(gamma), _p(theta), int(n0), _p(state_in),
+                                             _p(out), _p(state_out), B, H, N, dk, dv, int(chunk), _stream(stream)))
     return out, state_out
 
 
@@ -383,6 +402,27 @@ def _step(fn, dtype, q, k, v, state, out, stream):
 def retention_step(q, k, v, state, out=None, stream=None):
     """One bf16 decode step; updates `state` in place and returns out."""
     return _step("retention_step", torch.bfloat16, q, k, v, state, out, stream)
+
+
+def retention_step_rotated(q, k, v, theta, pos: int, state, out=None, stream=None):
+    """One bf16 decode step of the token at position `pos`, q and k turned by
+    the position phase rotation first; updates `state` in place, returns out."""
+    if q.dim() != 3:
+        raise ValueError("q, k, v must be [B, H, d] for a step")
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _need(q, "q", torch.bfloat16, (B, H, dk))
+    _need(k, "k", torch.bfloat16, (B, H, dk))
+    _need(v, "v", torch.bfloat16, (B, H, dv))
+    _need(theta, "theta", torch.float32, (dk // 2,))
+    _need(state, "state", torch.float32, (B, H, dk, dv))
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, H, dv))
+    _check("retention_step_rotated",
+           lib().retention_step_rotated(_p(q), _p(k), _p(v), _p(theta), int(pos), _p(state), _p(out), B, H, dk, dv,
+                                        _stream(stream)))
+    return out
 
 
 def retention_step_f32(q, k, v, state, out=None, stream=None):

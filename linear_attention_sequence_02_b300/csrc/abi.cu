@@ -78,7 +78,8 @@ int plan_chunkwise(int B, int H, int N, int dk, int dv, int chunk, int sms, ret:
 // stream-ordered (cudaMallocAsync / cudaFreeAsync on the call's stream).
 int chunkwise_alloc(const void* q, const void* k, const void* v, const float* gamma,
                     const float* state_in, void* out, float* state_out, int B, int H, int N, int dk,
-                    int dv, int chunk, const ret::ChunkNorm* norm, void* stream) {
+                    int dv, int chunk, const ret::ChunkNorm* norm, void* stream,
+                    const ret::ChunkRotation* rot = nullptr) {
   int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
   if (st != RET_OK) return st;
   ret::ChunkPlan plan;
@@ -102,7 +103,7 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
       return RET_ERR_CUDA;
   }
   cudaError_t e = ret::launch_chunk_tc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, plan, ws,
-                                       norm, 0.f, s);
+                                       norm, 0.f, s, rot);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = e2;
@@ -251,6 +252,19 @@ int retention_chunkwise_from_state(const void* q, const void* k, const void* v, 
   return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream);
 }
 
+int retention_chunkwise_rotated(const void* q, const void* k, const void* v, const float* gamma, const float* theta,
+                                int n0, const float* state_in, void* out, float* state_out, int B, int H, int N,
+                                int dk, int dv, int chunk, void* stream) {
+  if (!theta || !aligned(theta, 4) || n0 < 0) return RET_ERR_INVALID;
+  if (state_in && (!aligned(state_in, 16) || state_in == state_out)) return RET_ERR_INVALID;
+  // every row of every tile, padding included, at an exact float position
+  const int tile = chunk == 32 ? 64 : chunk;
+  if (chunk > 0 && N >= 0 && (int64_t)n0 + ((int64_t)N + tile - 1) / tile * tile > (1 << 24))
+    return RET_ERR_UNSUPPORTED;
+  const ret::ChunkRotation rot{theta, n0};
+  return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream, &rot);
+}
+
 int retention_chunkwise_groupnorm(const void* q, const void* k, const void* v, const float* gamma,
                                   const float* weight, const float* bias, float eps, void* out,
                                   float* state_out, int B, int H, int N, int dk, int dv, int chunk,
@@ -368,6 +382,17 @@ int retention_step(const void* q, const void* k, const void* v, float* state, vo
   if (dv > 4 * 65535 * 32) return RET_ERR_UNSUPPORTED;
   return from_cuda(ret::launch_step_bf16(q, k, v, state, out, B, H, dk, dv,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+int retention_step_rotated(const void* q, const void* k, const void* v, const float* theta, int pos,
+                           float* state, void* out, int B, int H, int dk, int dv, void* stream) {
+  int st = check_step(q, k, v, state, out, B, H, dk, dv);
+  if (st != RET_OK) return st;
+  if (!theta || !aligned(theta, 4) || pos < 0) return RET_ERR_INVALID;
+  if (pos >= (1 << 24) || dk % 2 != 0) return RET_ERR_UNSUPPORTED;
+  if (dv > 4 * 65535 * 32) return RET_ERR_UNSUPPORTED;
+  return from_cuda(ret::launch_step_bf16(q, k, v, state, out, B, H, dk, dv, static_cast<cudaStream_t>(stream), theta,
+                                         pos));
 }
 
 int retention_step_f32(const float* q, const float* k, const float* v, float* state, float* out,

@@ -68,6 +68,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "angle.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "retention.h"
@@ -109,7 +110,7 @@ struct Cfg {
   static constexpr int kV = C * DVT * 2;              // V_i slab (also W_i, then the output staging)
   static constexpr int kSb = SO ? 0 : 128 * DVT * 2;  // bf16 snapshot of one state half
   static constexpr int kPw = ((C + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kBarBytes = 64 * 8;
+  static constexpr int kBarBytes = 80 * 8;
   static constexpr int kStg = SO ? 0 : C * DVT * 2;   // output tile staging for the TMA store
   static constexpr int bytes(int nqk, int nv, int nsb, int nstg) {
     return nqk * kQK + nv * kV + nsb * kSb + nstg * kStg + kPw + kBarBytes + 16 + 1024;  // + slack to align
@@ -174,7 +175,7 @@ struct Cfg {
                        bSbReady = bSFull + H, bSbFree = bSbReady + NSB, bPFull = bSbFree + NSB,
                        bPFree = bPFull + NP, bPtReady = bPFree + NP, bOFull = bPtReady + NP,
                        bOFree = bOFull + NO, bFin = bOFree + NO, bSDone = bFin + 1, bNever = bSDone + NV,
-                       kBars = bNever + 1;
+                       bQkRot = bNever + 1, kBars = bQkRot + NQK;
   static_assert(kBars * 8 <= kBarBytes, "barriers");
 };
 
@@ -190,6 +191,8 @@ struct TcParams {
   int dk;            // query/key width (<= DK; the columns past it are zero-filled by the loads)
   float scale;       // factor of the query (1/sqrt(dk) unless the caller sets another)
   unsigned int test_stall_us;  // > 0: failure-path test (see retention_test_stall_waits)
+  const float* theta;  // rotation kernels: frequencies [dk/2] of the position phase rotation
+  int n0;              //   and the position of token 0
 };
 
 // Position of this CTA: value tile, head (b*H+h) and sequence segment, value
@@ -402,7 +405,7 @@ __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, u
     const float4* src = reinterpret_cast<const float4*>(sm);
     float* base = p.state_out + (size_t)bh * p.dk * p.dv + dv0;
     const int cols4 = min(DVT, p.dv - dv0) / 4;  // value columns of this tile inside dv
-    for (int q4 = threadIdx.x; q4 < p.dk * cols4; q4 += kThreads) {
+    for (int q4 = threadIdx.x; q4 < p.dk * cols4; q4 += blockDim.x) {
       const int row = q4 / cols4, c4 = q4 % cols4;
       *reinterpret_cast<float4*>(base + (size_t)row * p.dv + 4 * c4) = src[row * (L::kStageRow / 4) + c4];
     }
@@ -420,7 +423,7 @@ struct RoleCtx {
 // The four roles of a CTA (producer, MMA issuer, state group, output group).
 // FAST selects the rescaled form; a CTA picks one instantiation at its start,
 // so the code it runs holds no branches of the other form.
-template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM>
+template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM, bool ROT>
 __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x) {
   using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
@@ -595,7 +598,8 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       const uint64_t dKa = make_sdesc(qk_k(0), C * 128, 1024);    // K^T, MN-major A (state)
       const uint64_t dV = make_sdesc(v_slot(0), C * 128, 1024);   // W or V, MN-major B
       const uint64_t dSb = make_sdesc(sb_buf(0), 128 * 128, 1024);  // snapshot, MN-major B
-      const uint32_t bQkFull = bar(L::bQkFull), bQkEmpty = bar(L::bQkEmpty), bVFull = bar(L::bVFull),
+      // Q/K slots are ready once loaded, or, with the rotation group, once turned
+      const uint32_t bQkFull = bar(ROT ? L::bQkRot : L::bQkFull), bQkEmpty = bar(L::bQkEmpty), bVFull = bar(L::bVFull),
                      bVEmpty = bar(L::bVEmpty), bWReady = bar(L::bWReady), bSRead = bar(L::bSRead),
                      bSFull = bar(L::bSFull), bSbReady = bar(L::bSbReady), bSbFree = bar(L::bSbFree),
                      bPFull = bar(L::bPFull), bPFree = bar(L::kMergePFree ? L::bOFull : L::bPFree),
@@ -770,7 +774,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       if (SO) {
         for (int hh = 0; hh < H; ++hh) {
           const int u = i * H + hh;
-          if (!gw(L::bQkFull + u % NQK, (u / NQK) & 1)) return false;
+          if (!gw((ROT ? L::bQkRot : L::bQkFull) + u % NQK, (u / NQK) & 1)) return false;
         }
       } else if (!gw(L::bPFull + i % NP, (i / NP) & 1)) {
         return false;
@@ -920,15 +924,74 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       }
     }
     if (et == 0) *reinterpret_cast<float*>(sm + L::oCState) = c;
-  } else if (!SO) {
+  } else {
     // ================= output group (warps 6..9) =================
     const int eo = threadIdx.x - 192;
     const int quarter = warp & 3;
     const uint32_t lane_addr = (uint32_t)(32 * quarter) << 16;
     const int arow = acc_row(C, quarter, lane);  // token row of the C-row accumulators, -1 if none
-    if (!zero_init) init_state(32 * quarter + lane, lane_addr, DVT / 64, DVT / 32);
+    if (!SO && !zero_init) init_state(32 * quarter + lane, lane_addr, DVT / 64, DVT / 32);
     auto go = [&](int b, uint32_t par) { return group_wait(kBarO, bar(b), par, abort_flag); };
     bool alive = true;
+
+    // Rotation kernels: the position phase rotation of the queries and keys
+    // of each Q/K slot, in place, once the slot has landed and before the MMA
+    // issuers read it ("2. Relative Position via Complex Exponential Phase
+    // Rotations": pair (2j, 2j+1) of the token at position n0 + n turned by
+    // (n0 + n) theta_j, the angle reduced modulo 2 pi as in the standalone
+    // rotation).  Thread eo owns the 16-byte unit c16 = eo % 16 (pairs
+    // 4 c16 .. 4 c16 + 3 of a 128-column half) of rows eo / 16 + 8 m, so it
+    // loads its frequencies once.  The state-only pass turns keys only.
+    float th[H][4];
+    RingPos<NQK> qk_rot;
+    if constexpr (ROT) {
+#pragma unroll
+      for (int hh = 0; hh < H; ++hh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = hh * 64 + 4 * (eo & 15) + e;
+          th[hh][e] = 2 * j < p.dk ? __ldg(p.theta + j) : 0.f;
+        }
+    }
+    auto rotate_chunk = [&](int i) -> bool {
+      if constexpr (ROT) {
+        const int c16 = eo & 15;
+#pragma unroll 1
+        for (int hh = 0; hh < H; ++hh) {
+          if (!go(L::bQkFull + qk_rot.slot, qk_rot.phase)) return false;
+          uint8_t* qs = sm + qk_rot.slot * L::kQK;
+          uint8_t* ks = qs + L::kQ;
+          const int pos0 = p.n0 + (c_begin + i) * C;
+#pragma unroll 1
+          for (int row = eo >> 4; row < C; row += kGroup / 16) {
+            const float pos = (float)(pos0 + row);
+            float cs[4], sn[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) __sincosf(reduced_angle(pos, th[hh][e]), &sn[e], &cs[e]);
+            const uint32_t off = (uint32_t)((c16 >> 3) * C * 128) + swz128(row, c16 & 7);
+            if (!SO) {
+              uint4 v = *reinterpret_cast<const uint4*>(qs + off);
+              v = make_uint4(rot_pair(v.x, cs[0], sn[0]), rot_pair(v.y, cs[1], sn[1]), rot_pair(v.z, cs[2], sn[2]),
+                             rot_pair(v.w, cs[3], sn[3]));
+              *reinterpret_cast<uint4*>(qs + off) = v;
+            }
+            uint4 w = *reinterpret_cast<const uint4*>(ks + off);
+            w = make_uint4(rot_pair(w.x, cs[0], sn[0]), rot_pair(w.y, cs[1], sn[1]), rot_pair(w.z, cs[2], sn[2]),
+                           rot_pair(w.w, cs[3], sn[3]));
+            *reinterpret_cast<uint4*>(ks + off) = w;
+          }
+          fence_proxy_async_smem();  // the MMAs read the turned pairs through the async proxy
+          mbar_arrive(bar(L::bQkRot + qk_rot.slot));
+          qk_rot.next();
+        }
+      }
+      return true;
+    };
+    if constexpr (SO) {
+      // state-only pass: this group has nothing else to do
+      if constexpr (ROT)
+        for (int i = 0; i < nck && alive; ++i) alive = rotate_chunk(i);
+    } else {
     if (p.test_stall_us > 0) {
       // Failure-path test: one wait on a barrier nothing completes, with a
       // short limit; it gives up, raises the abort flag and sets the device
@@ -1073,21 +1136,32 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
 
     float c = 1.f;
     int n = 0;
+    // Rotation kernels.  With lookahead, chunks 0 and 1 are turned first and
+    // chunk i+2 between the mask of chunk i+1 and the outputs of chunk i, so
+    // its Q K^T issues while this group writes outputs.  Without it (one
+    // chunk's Q/K in the ring, or one P buffer), chunk i at the top of its
+    // iteration, once its slot has been reloaded.
+    if (ROT && look) {
+      for (int i = 0; i < 2 && i < nck && alive; ++i) alive = rotate_chunk(i);
+    }
     if (look) {
       for (int i = -1; i < nck && alive; ++i) {
         if (i + 1 < nck && !ptilde(i + 1)) { alive = false; break; }
+        if (ROT && i + 2 < nck && i >= 0 && !rotate_chunk(i + 2)) { alive = false; break; }
         if (i < 0) continue;
         if (fast) frame_advance(c, n, inv_g(i));
         if (!out_chunk(i, c)) { alive = false; break; }
       }
     } else {
       for (int i = 0; i < nck && alive; ++i) {
+        if (ROT && !rotate_chunk(i)) { alive = false; break; }
         if (!ptilde(i)) { alive = false; break; }
         if (fast) frame_advance(c, n, inv_g(i));
         if (!out_chunk(i, c)) { alive = false; break; }
       }
     }
     if (eo == 0) bulk_wait_group0();
+    }
   }
 
 }
@@ -1126,9 +1200,10 @@ __device__ __forceinline__ void init_barriers(uint32_t sbase) {
   mbar_init(bar(L::bFin), SO ? 1 : 2);
   for (int i = 0; i < L::NV; ++i) mbar_init(bar(L::bSDone + i), 1);
   mbar_init(bar(L::bNever), 1);  // nothing ever arrives here (failure-path test)
+  for (int i = 0; i < L::NQK; ++i) mbar_init(bar(L::bQkRot + i), kGroup);
 }
 
-template <int C, int DK, int DVT, bool SO, bool NORM>
+template <int C, int DK, int DVT, bool SO, bool NORM, bool ROT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -1163,7 +1238,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
-  for (int d = threadIdx.x; d <= C; d += kThreads) pw[d] = gamma_pow(g, lg, (float)d);
+  for (int d = threadIdx.x; d <= C; d += blockDim.x) pw[d] = gamma_pow(g, lg, (float)d);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1175,8 +1250,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   if (SO) griddep_launch_dependents();
 
   const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC};
-  if (fast) chunk_roles<C, DK, DVT, SO, true, NORM>(p, x);
-  else chunk_roles<C, DK, DVT, SO, false, NORM>(p, x);
+  if (fast) chunk_roles<C, DK, DVT, SO, true, NORM, ROT>(p, x);
+  else chunk_roles<C, DK, DVT, SO, false, NORM, ROT>(p, x);
 
   // ---- teardown: every MMA has completed, every load landed, every store read ----
   tc_fence_before();
@@ -1247,11 +1322,11 @@ bool make_map_heads(CUtensorMap* m, const void* base, int dv, int H, int N, int 
   return r == CUDA_SUCCESS;
 }
 
-template <int C, int DK, int DVT, bool SO, bool NORM>
+template <int C, int DK, int DVT, bool SO, bool NORM, bool ROT>
 cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mo, const TcParams& p, int grid, bool pdl, cudaStream_t s) {
   using L = Cfg<C, DK, DVT, SO>;
-  auto kern = chunk_tc_kernel<C, DK, DVT, SO, NORM>;
+  auto kern = chunk_tc_kernel<C, DK, DVT, SO, NORM, ROT>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -1280,16 +1355,31 @@ cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return cudaGetLastError();
 }
 
-template <int C, int DK, int DVT, bool NORM>
+template <int C, int DK, int DVT, bool NORM, bool ROT>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   const bool split = p.segments > 1;
   if (split) {
-    cudaError_t e = launch_one<C, DK, DVT, true, false>(mq, mk, mv, mo, p, p.BH * (p.segments - 1) * p.n_dv_tiles,
-                                                        false, s);
+    cudaError_t e = launch_one<C, DK, DVT, true, false, ROT>(mq, mk, mv, mo, p,
+                                                             p.BH * (p.segments - 1) * p.n_dv_tiles, false, s);
     if (e != cudaSuccess) return e;
   }
-  return launch_one<C, DK, DVT, false, NORM>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
+  return launch_one<C, DK, DVT, false, NORM, ROT>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
+}
+
+// The variant for these tile sizes.
+template <bool NORM, bool ROT>
+cudaError_t launch_variant(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
+  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+  return cudaErrorNotSupported;
 }
 
 // The value-tile width used for these sizes.
@@ -1337,11 +1427,12 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H, int N,
                             int dk, int dv, const ChunkPlan& plan, float* workspace,
-                            const ChunkNorm* norm, float scale, cudaStream_t s) {
+                            const ChunkNorm* norm, float scale, cudaStream_t s, const ChunkRotation* rot) {
   const int BH = B * H;
   const int chunk = plan.chunk;
   // GroupNorm statistics need a head's whole row, unpadded, in one CTA
   if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv)) return cudaErrorNotSupported;
+  if (norm && rot) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, q, dk, N, BH, chunk) || !make_map(&mk, k, dk, N, BH, chunk) ||
       !make_map(&mv, v, dv, N, BH, chunk) ||
@@ -1366,28 +1457,13 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.n_chunks = plan.n_chunks;
   p.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)dk));
   p.test_stall_us = g_test_stall_us.load(std::memory_order_relaxed);
+  p.theta = rot ? rot->theta : nullptr;
+  p.n0 = rot ? rot->n0 : 0;
   const bool t128 = plan.dvt == 128;
   const int dkt = plan.dk_tile;
-  if (norm) {
-    if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, true>(mq, mk, mv, mo, p, s)
-                                               : launch_pair<64, 128, 64, true>(mq, mk, mv, mo, p, s);
-    if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, true>(mq, mk, mv, mo, p, s)
-                                                : launch_pair<128, 128, 64, true>(mq, mk, mv, mo, p, s);
-    if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, true>(mq, mk, mv, mo, p, s)
-                                               : launch_pair<64, 256, 64, true>(mq, mk, mv, mo, p, s);
-    if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, true>(mq, mk, mv, mo, p, s)
-                                                : launch_pair<128, 256, 64, true>(mq, mk, mv, mo, p, s);
-    return cudaErrorNotSupported;
-  }
-  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, false>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<64, 128, 64, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, false>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<128, 128, 64, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, false>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<64, 256, 64, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, false>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<128, 256, 64, false>(mq, mk, mv, mo, p, s);
-  return cudaErrorNotSupported;
+  if (norm) return launch_variant<true, false>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
+  if (rot) return launch_variant<false, true>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
+  return launch_variant<false, false>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
 }
 
 cudaError_t read_device_status(unsigned int* flags, int clear) {

@@ -15,8 +15,11 @@ constexpr int kMaxSmemPerBlock = 232448;  // 227 KB
 
 // ---- SIMT kernels (simt.cu) -------------------------------------------------
 // Each returns a cudaError_t from the launch (cudaGetLastError after it).
+// theta (nullable): q and k are first turned by the position phase rotation
+// of the token at position pos.
 cudaError_t launch_step_bf16(const void* q, const void* k, const void* v, float* state, void* out,
-                             int B, int H, int dk, int dv, cudaStream_t s);
+                             int B, int H, int dk, int dv, cudaStream_t s, const float* theta = nullptr,
+                             int pos = 0);
 cudaError_t launch_step_f32(const float* q, const float* k, const float* v, float* state,
                             float* out, int B, int H, int dk, int dv, cudaStream_t s);
 cudaError_t launch_parallel_bf16(const void* q, const void* k, const void* v, const float* gamma,
@@ -58,13 +61,20 @@ struct ChunkNorm {
   const float* bias;
   float eps;
 };
+// Position phase rotation applied to q and k inside the kernel: frequencies
+// theta [dk/2] (device), position of token 0.
+struct ChunkRotation {
+  const float* theta;
+  int n0;
+};
 // state_in (nullable) is the state before the first token, [B*H][dk][dv];
 // norm (nullable) selects the GroupNorm epilogue; scale multiplies the query
-// (<= 0: 1/sqrt(dk)).
+// (<= 0: 1/sqrt(dk)); rot (nullable) turns q and k by their positions first.
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H,
                             int N, int dk, int dv, const ChunkPlan& plan, float* workspace,
-                            const ChunkNorm* norm, float scale, cudaStream_t s);
+                            const ChunkNorm* norm, float scale, cudaStream_t s,
+                            const ChunkRotation* rot = nullptr);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 // Failure-path test setting read by every chunkwise launch (0: off).
 extern std::atomic<unsigned int> g_test_stall_us;

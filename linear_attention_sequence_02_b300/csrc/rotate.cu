@@ -23,6 +23,7 @@
 
 #include <cstdint>
 
+#include "angle.cuh"
 #include "internal.h"
 
 namespace ret {
@@ -30,28 +31,6 @@ namespace {
 
 constexpr int kRotThreads = 256;
 constexpr int kRotInFlight = 4;  // (b, h) rows a thread loads before it rotates any
-
-// 2 pi = kTwoPiHi + kTwoPiLo + ~7e-15: kTwoPiHi is 2 pi rounded to float,
-// kTwoPiLo the remainder rounded to float.
-constexpr float kTwoPiHi = 0x1.921fb6p+2f;
-constexpr float kTwoPiLo = -0x1.777a5cp-23f;
-constexpr float kInvTwoPi = 0x1.45f306p-3f;
-
-// angle p theta reduced to about [-pi, pi]; p is an integer below 2^24 (exact)
-__device__ __forceinline__ float reduced_angle(float p, float theta) {
-  const float hi = p * theta;
-  const float lo = fmaf(p, theta, -hi);  // p theta = hi + lo exactly
-  const float k = rintf(hi * kInvTwoPi);
-  float r = fmaf(-k, kTwoPiHi, hi);  // exact: the difference needs at most 24 bits
-  r = fmaf(-k, kTwoPiLo, r);
-  return r + lo;
-}
-
-__device__ __forceinline__ uint32_t rot_pair(uint32_t w, float c, float s) {
-  const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-  const __nv_bfloat162 o = __floats2bfloat162_rn(v.x * c - v.y * s, v.x * s + v.y * c);
-  return *reinterpret_cast<const uint32_t*>(&o);
-}
 
 __global__ void __launch_bounds__(kRotThreads)
 rotate_kernel(const __nv_bfloat16* x, const float* __restrict__ theta, __nv_bfloat16* y, int BH, int N,

@@ -15,6 +15,7 @@
 
 #include <cstdint>
 
+#include "angle.cuh"
 #include "internal.h"
 
 namespace ret {
@@ -54,6 +55,10 @@ __device__ __forceinline__ float decay_pow(float g, float lg, int d) {
 // written so that eight 16-byte loads per thread are in flight.  The column
 // partial sums of q~ . S' are reduced across the 8 warps in shared memory.
 // gamma_h = 1 - 2^(-5-h) is formed exactly in fp32 from the head index.
+// With a rotation (theta non-null), q and k are first turned by the token's
+// position ("2. Relative Position via Complex Exponential Phase Rotations":
+// pair (2j, 2j+1) by pos theta_j, the angle reduced modulo 2 pi by the method
+// of Cody and Waite), in fp32, as they are loaded.
 constexpr int kStepThreads = 256;
 constexpr int kStepCols = 128;
 constexpr int kStepUnroll = 8;
@@ -61,7 +66,8 @@ constexpr int kStepUnroll = 8;
 template <typename T>
 __global__ void __launch_bounds__(kStepThreads)
 step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-            float* __restrict__ state, T* __restrict__ out, int H, int dk, int dv) {
+            float* __restrict__ state, T* __restrict__ out, int H, int dk, int dv,
+            const float* __restrict__ theta, int pos) {
   extern __shared__ float sm[];
   float* qs = sm;               // [dk]  q / sqrt(dk)
   float* ks = sm + dk;          // [dk]
@@ -70,9 +76,22 @@ step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
   const int h = bh % H;
   const float g = 1.0f - ldexpf(1.0f, -5 - h);
   const float scale = 1.0f / sqrtf((float)dk);
-  for (int i = threadIdx.x; i < dk; i += kStepThreads) {
-    qs[i] = to_f32(q[(size_t)bh * dk + i]) * scale;
-    ks[i] = to_f32(k[(size_t)bh * dk + i]);
+  if (theta == nullptr) {
+    for (int i = threadIdx.x; i < dk; i += kStepThreads) {
+      qs[i] = to_f32(q[(size_t)bh * dk + i]) * scale;
+      ks[i] = to_f32(k[(size_t)bh * dk + i]);
+    }
+  } else {
+    for (int j = threadIdx.x; 2 * j < dk; j += kStepThreads) {
+      float sn, cs;
+      sincosf(reduced_angle((float)pos, __ldg(theta + j)), &sn, &cs);
+      const float q0 = to_f32(q[(size_t)bh * dk + 2 * j]), q1 = to_f32(q[(size_t)bh * dk + 2 * j + 1]);
+      const float k0 = to_f32(k[(size_t)bh * dk + 2 * j]), k1 = to_f32(k[(size_t)bh * dk + 2 * j + 1]);
+      qs[2 * j] = (q0 * cs - q1 * sn) * scale;
+      qs[2 * j + 1] = (q0 * sn + q1 * cs) * scale;
+      ks[2 * j] = k0 * cs - k1 * sn;
+      ks[2 * j + 1] = k0 * sn + k1 * cs;
+    }
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,7 +142,7 @@ step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
 
 template <typename T>
 cudaError_t launch_step(const T* q, const T* k, const T* v, float* state, T* out, int B, int H,
-                        int dk, int dv, cudaStream_t s) {
+                        int dk, int dv, cudaStream_t s, const float* theta = nullptr, int pos = 0) {
   const size_t smem = sizeof(float) * (2 * (size_t)dk + 8 * kStepCols);
   auto kern = step_kernel<T>;
   if (smem > 48 * 1024) {
@@ -132,7 +151,7 @@ cudaError_t launch_step(const T* q, const T* k, const T* v, float* state, T* out
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)(B * H), (unsigned)((dv + kStepCols - 1) / kStepCols));
-  kern<<<grid, kStepThreads, smem, s>>>(q, k, v, state, out, H, dk, dv);
+  kern<<<grid, kStepThreads, smem, s>>>(q, k, v, state, out, H, dk, dv, theta, pos);
   return cudaGetLastError();
 }
 
@@ -332,10 +351,10 @@ chunkwise_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 }  // namespace
 
 cudaError_t launch_step_bf16(const void* q, const void* k, const void* v, float* state, void* out,
-                             int B, int H, int dk, int dv, cudaStream_t s) {
+                             int B, int H, int dk, int dv, cudaStream_t s, const float* theta, int pos) {
   return launch_step(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                      static_cast<const __nv_bfloat16*>(v), state, static_cast<__nv_bfloat16*>(out),
-                     B, H, dk, dv, s);
+                     B, H, dk, dv, s, theta, pos);
 }
 
 cudaError_t launch_step_f32(const float* q, const float* k, const float* v, float* state,
