@@ -605,6 +605,15 @@ def parallel_entry(w, reps, dev, flush, tflops):
             "gpu_launches": 1}
 
 
+def oracle_sample(w, seed=0):
+    """One batch row of workload `w` (all H heads) as fp64 arrays for the oracle."""
+    from linear_attention_sequence_02_b300 import binding, inputs
+    H, N, dk, dv = w["H"], w["N"], w["dk"], w["dv"]
+    q, k, v = inputs.qkv(1, H, N, dk, dv, seed, torch.bfloat16)
+    g = binding.gamma_schedule(H).double().numpy()
+    return tuple(x.double().numpy() for x in (q, k, v)) + (g,)
+
+
 def cpu_baseline_chunkwise(w, min_seconds=10.0, max_passes=30):
     """fp64 oracle (chunkwise form, same chunk) on one batch row of the
     workload (all its heads), repeated for >= min_seconds; tokens/s of the
