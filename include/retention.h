@@ -125,10 +125,15 @@ int retention_chunkwise_from_state(const void *q, const void *k, const void *v, 
  * retention_chunkwise_rotated -- retention_chunkwise_from_state of the queries
  * and keys turned by the position phase rotation of "2. Relative Position via
  * Complex Exponential Phase Rotations" (as retention_rotate below, with the
- * same theta and n0 for q and k), the rotation fused into the kernels' load
- * stage: each Q/K tile is turned in shared memory after it lands and before
- * the tensor cores read it, so q and k are read from HBM once and the turned
- * copies are never written:
+ * same theta and n0 for q and k).  With 64-token tiles (chunk 32 or 64) and
+ * one value tile per head (dv of at most 64, or exactly 128), the
+ * rotation is fused into the kernels' load stage: each Q/K tile is turned in
+ * shared memory after it lands and before the tensor cores read it, so q and
+ * k are read from HBM once and the turned copies are never written.  For
+ * other shapes (128-token tiles, several value tiles per head) that fusion
+ * measured slower than separate passes, so q and k are turned into a
+ * stream-ordered scratch buffer (cudaMallocAsync / cudaFreeAsync on
+ * `stream`) by the standalone rotation first.  Either way:
  *
  *   out = chunkwise(rotate(q, theta, n0), rotate(k, theta, n0), v, gamma; state_in)
  *

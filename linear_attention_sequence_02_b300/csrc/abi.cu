@@ -262,7 +262,34 @@ int retention_chunkwise_rotated(const void* q, const void* k, const void* v, con
   if (chunk > 0 && N >= 0 && (int64_t)n0 + ((int64_t)N + tile - 1) / tile * tile > (1 << 24))
     return RET_ERR_UNSUPPORTED;
   const ret::ChunkRotation rot{theta, n0};
-  return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream, &rot);
+  // Where the rotation is fused, the output group turns each Q/K slot in
+  // shared memory.  That pays with 64-token tiles and one value tile per head;
+  // with 128-token tiles, or several value-tile CTAs per head (each would turn
+  // the same Q/K tiles), the extra instructions on that latency-bound group
+  // cost more than the HBM traffic they save, so q and k are turned by the
+  // standalone pass into scratch first.
+  int st = check_sequence(q, k, v, gamma, out, state_out, B, H, N, dk, dv);
+  if (st != RET_OK) return st;
+  ret::ChunkPlan plan;
+  const int sms = num_sms();
+  if (sms <= 0) return RET_ERR_CUDA;
+  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
+  if (st != RET_OK) return st;
+  if (N == 0 || (plan.chunk == 64 && plan.n_dv_tiles == 1))
+    return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream, &rot);
+  if (!ret::rotate_supported(N, dk, n0)) return RET_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)B * H * N * dk * 2;  // one turned copy of q or k (bf16)
+  char* scratch = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), 2 * bytes, s) != cudaSuccess) return RET_ERR_CUDA;
+  cudaError_t e = ret::launch_rotate_bf16(q, theta, scratch, B, H, N, dk, n0, s);
+  if (e == cudaSuccess) e = ret::launch_rotate_bf16(k, theta, scratch + bytes, B, H, N, dk, n0, s);
+  int r = from_cuda(e);
+  if (r == RET_OK)
+    r = chunkwise_alloc(scratch, scratch + bytes, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr,
+                        stream);
+  const cudaError_t e2 = cudaFreeAsync(scratch, s);
+  return r != RET_OK ? r : from_cuda(e2);
 }
 
 int retention_chunkwise_groupnorm(const void* q, const void* k, const void* v, const float* gamma,

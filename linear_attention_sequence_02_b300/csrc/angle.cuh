@@ -4,7 +4,6 @@
 // of the query or key of the token at position p is turned by p theta_j.
 #pragma once
 
-#include <cuda_bf16.h>
 #include <cstdint>
 
 namespace ret {
@@ -27,12 +26,16 @@ __device__ __forceinline__ float reduced_angle(float p, float theta) {
   return r + lo;
 }
 
-// One bf16 pair (x, y) turned by the angle with cosine c and sine s, rounded
-// to bf16 (round to nearest even).
+// One bf16 pair (x in the low half, y in the high half) turned by the angle
+// with cosine c and sine s, rounded to bf16 (round to nearest even).  A bf16
+// is the upper half of the float with the same bits, so unpacking is a shift
+// and a mask.
 __device__ __forceinline__ uint32_t rot_pair(uint32_t w, float c, float s) {
-  const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-  const __nv_bfloat162 o = __floats2bfloat162_rn(v.x * c - v.y * s, v.x * s + v.y * c);
-  return *reinterpret_cast<const uint32_t*>(&o);
+  const float x = __uint_as_float(w << 16), y = __uint_as_float(w & 0xffff0000u);
+  const float ox = fmaf(x, c, -y * s), oy = fmaf(x, s, y * c);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(oy), "f"(ox));  // oy to the high half
+  return r;
 }
 
 }  // namespace ret

@@ -938,47 +938,74 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     // of each Q/K slot, in place, once the slot has landed and before the MMA
     // issuers read it ("2. Relative Position via Complex Exponential Phase
     // Rotations": pair (2j, 2j+1) of the token at position n0 + n turned by
-    // (n0 + n) theta_j, the angle reduced modulo 2 pi as in the standalone
-    // rotation).  Thread eo owns the 16-byte unit c16 = eo % 16 (pairs
-    // 4 c16 .. 4 c16 + 3 of a 128-column half) of rows eo / 16 + 8 m, so it
-    // loads its frequencies once.  The state-only pass turns keys only.
-    float th[H][4];
+    // (n0 + n) theta_j).  Thread eo owns the 16-byte unit c16 = eo % 16
+    // (pairs 4 c16 .. 4 c16 + 3 of a 128-column half) of rows eo / 16 + 8 m.
+    // Per slot it takes the cosine and sine of its first row's angle, reduced
+    // modulo 2 pi as in the standalone rotation, and advances them 8 rows at
+    // a time by the rotation through 8 theta_j (at most 16 steps, ~1e-7 of
+    // rounding each), four rows per batch with every load of a batch issued
+    // before any store.  The state-only pass turns keys only.
     RingPos<NQK> qk_rot;
-    if constexpr (ROT) {
-#pragma unroll
-      for (int hh = 0; hh < H; ++hh)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = hh * 64 + 4 * (eo & 15) + e;
-          th[hh][e] = 2 * j < p.dk ? __ldg(p.theta + j) : 0.f;
-        }
-    }
     auto rotate_chunk = [&](int i) -> bool {
       if constexpr (ROT) {
-        const int c16 = eo & 15;
+        const int c16 = eo & 15, r0 = eo >> 4;
+        constexpr int kStep = kGroup / 16;  // rows between a thread's rows
+        constexpr int kRows = 4;            // rows per batch: every load of a batch before any store
+        static_assert(C % (kRows * kStep) == 0, "rotation batches");
 #pragma unroll 1
         for (int hh = 0; hh < H; ++hh) {
           if (!go(L::bQkFull + qk_rot.slot, qk_rot.phase)) return false;
           uint8_t* qs = sm + qk_rot.slot * L::kQK;
           uint8_t* ks = qs + L::kQ;
-          const int pos0 = p.n0 + (c_begin + i) * C;
-#pragma unroll 1
-          for (int row = eo >> 4; row < C; row += kGroup / 16) {
-            const float pos = (float)(pos0 + row);
-            float cs[4], sn[4];
+          // this half's frequencies and the rotation through kStep rows (kept
+          // in registers: arrays shared with the rest of the role would live
+          // in memory)
+          float tj[4], cj[4], sj[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) __sincosf(reduced_angle(pos, th[hh][e]), &sn[e], &cs[e]);
-            const uint32_t off = (uint32_t)((c16 >> 3) * C * 128) + swz128(row, c16 & 7);
-            if (!SO) {
-              uint4 v = *reinterpret_cast<const uint4*>(qs + off);
-              v = make_uint4(rot_pair(v.x, cs[0], sn[0]), rot_pair(v.y, cs[1], sn[1]), rot_pair(v.z, cs[2], sn[2]),
-                             rot_pair(v.w, cs[3], sn[3]));
-              *reinterpret_cast<uint4*>(qs + off) = v;
+          for (int e = 0; e < 4; ++e) {
+            const int j = hh * 64 + 4 * c16 + e;
+            tj[e] = 2 * j < p.dk ? __ldg(p.theta + j) : 0.f;
+            const float a = reduced_angle((float)kStep, tj[e]);
+            sj[e] = __sinf(a);
+            cj[e] = __cosf(a);
+          }
+          float ca[4], sa[4];
+          const float pos = (float)(p.n0 + (c_begin + i) * C + r0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = reduced_angle(pos, tj[e]);
+            sa[e] = __sinf(a);
+            ca[e] = __cosf(a);
+          }
+#pragma unroll 1
+          for (int row = r0; row < C; row += kRows * kStep) {
+            uint32_t off[kRows];
+            uint4 vq[kRows], vk[kRows];
+#pragma unroll
+            for (int t = 0; t < kRows; ++t) {
+              off[t] = (uint32_t)((c16 >> 3) * C * 128) + swz128(row + t * kStep, c16 & 7);
+              if (!SO) vq[t] = *reinterpret_cast<const uint4*>(qs + off[t]);
+              vk[t] = *reinterpret_cast<const uint4*>(ks + off[t]);
             }
-            uint4 w = *reinterpret_cast<const uint4*>(ks + off);
-            w = make_uint4(rot_pair(w.x, cs[0], sn[0]), rot_pair(w.y, cs[1], sn[1]), rot_pair(w.z, cs[2], sn[2]),
-                           rot_pair(w.w, cs[3], sn[3]));
-            *reinterpret_cast<uint4*>(ks + off) = w;
+#pragma unroll
+            for (int t = 0; t < kRows; ++t) {
+              if (!SO)
+                vq[t] = make_uint4(rot_pair(vq[t].x, ca[0], sa[0]), rot_pair(vq[t].y, ca[1], sa[1]),
+                                   rot_pair(vq[t].z, ca[2], sa[2]), rot_pair(vq[t].w, ca[3], sa[3]));
+              vk[t] = make_uint4(rot_pair(vk[t].x, ca[0], sa[0]), rot_pair(vk[t].y, ca[1], sa[1]),
+                                 rot_pair(vk[t].z, ca[2], sa[2]), rot_pair(vk[t].w, ca[3], sa[3]));
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {  // advance kStep rows
+                const float cn = ca[e] * cj[e] - sa[e] * sj[e];
+                sa[e] = sa[e] * cj[e] + ca[e] * sj[e];
+                ca[e] = cn;
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < kRows; ++t) {
+              if (!SO) *reinterpret_cast<uint4*>(qs + off[t]) = vq[t];
+              *reinterpret_cast<uint4*>(ks + off[t]) = vk[t];
+            }
           }
           fence_proxy_async_smem();  // the MMAs read the turned pairs through the async proxy
           mbar_arrive(bar(L::bQkRot + qk_rot.slot));
@@ -1368,17 +1395,37 @@ cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 }
 
 // The variant for these tile sizes.
+template <bool NORM>
+cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s);
+
+// The fused rotation is built for 64-token tiles only (the shapes where it
+// pays; see retention_chunkwise_rotated).
 template <bool NORM, bool ROT>
 cudaError_t launch_variant(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
                                              : launch_pair<64, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<128, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
-  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<64, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<128, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+  if constexpr (ROT) {
+    if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<64, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+    return cudaErrorNotSupported;
+  } else {
+    return launch_variant_all<NORM>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
+  }
+}
+
+template <bool NORM>
+cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
+  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, false>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 128, 64, NORM, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, NORM, false>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 128, 64, NORM, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, false>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 256, 64, NORM, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, false>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 256, 64, NORM, false>(mq, mk, mv, mo, p, s);
   return cudaErrorNotSupported;
 }
 
