@@ -1404,9 +1404,9 @@ cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap&
 template <bool NORM, bool ROT>
 cudaError_t launch_variant(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
-  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<64, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
   if constexpr (ROT) {
+    if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<64, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
     if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
                                                : launch_pair<64, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
     return cudaErrorNotSupported;
