@@ -102,6 +102,7 @@ struct Cfg {
   static_assert(C == 64 || C == 128, "chunk");
   static_assert(DK == 128 || DK == 256, "dk");
   static_assert(DVT == 64 || DVT == 128, "value tile");
+  static constexpr int kC = C, kDVT = DVT;
   static constexpr int H = DK / 128;                  // 128-row halves of the state
   // shared memory
   static constexpr int kQ = SO ? 0 : C * 256;         // one 128-column half of Q_i: two 64-column boxes
@@ -418,7 +419,33 @@ struct RoleCtx {
   uint8_t* sm;
   uint32_t tmem;
   float inv_gC;  // 1 / gamma^C (rescaled form only)
+  int pre;       // leading chunks whose loads the set-up already issued
 };
+
+// TMA loads of chunk i into the ring slots of layout L: the V slab into V slot
+// i % NV, and Q/K half hh into Q/K slot (i H + hh) % NQK.  The caller has made
+// sure the slots are free.
+template <class L, bool SO>
+__device__ __forceinline__ void load_v(uint32_t sbase, const CUtensorMap* tmv, int i, int row, int dv0, int bh) {
+  const int s = i % L::NV;
+  const uint32_t full = sbase + L::oBar + 8 * (L::bVFull + s), dst = sbase + L::oV + s * L::kV;
+  mbar_arrive_expect_tx(full, L::kV);
+#pragma unroll
+  for (int b = 0; b < L::kDVT / 64; ++b) tma_load_3d(dst + b * L::kC * 128, tmv, dv0 + b * 64, row, bh, full);
+}
+template <class L, bool SO>
+__device__ __forceinline__ void load_qk(uint32_t sbase, const CUtensorMap* tmq, const CUtensorMap* tmk, int u, int hh,
+                                        int row, int bh) {
+  const int s = u % L::NQK;
+  const uint32_t full = sbase + L::oBar + 8 * (L::bQkFull + s), dst = sbase + s * L::kQK;
+  mbar_arrive_expect_tx(full, L::kQK);
+  if (!SO) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) tma_load_3d(dst + b * L::kC * 128, tmq, hh * 128 + b * 64, row, bh, full);
+  }
+#pragma unroll
+  for (int b = 0; b < 2; ++b) tma_load_3d(dst + L::kQ + b * L::kC * 128, tmk, hh * 128 + b * 64, row, bh, full);
+}
 
 // The four roles of a CTA (producer, MMA issuer, state group, output group).
 // FAST selects the rescaled form; a CTA picks one instantiation at its start,
@@ -536,9 +563,10 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
-      int v_issued = 0, qk_issued = 0;
+      // the set-up issued the loads of the first x.pre chunks
+      int v_issued = x.pre, qk_issued = x.pre * H;
       bool ok = true;
-      for (int i = 0; i < nck && ok; ++i) {
+      for (int i = x.pre; i < nck && ok; ++i) {
         const int row = (c_begin + i) * C;
         {
           const int s = i % NV, k = i / NV;
@@ -546,10 +574,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(L::bVFull + s), L::kV);
-#pragma unroll
-          for (int b = 0; b < DVT / 64; ++b)
-            tma_load_3d(v_slot(s) + b * C * 128, x.tmv, dv0 + b * 64, row, bh, bar(L::bVFull + s));
+          load_v<L, SO>(sbase, x.tmv, i, row, dv0, bh);
           v_issued = i + 1;
         }
         for (int hh = 0; hh < H; ++hh) {
@@ -558,15 +583,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(L::bQkFull + s), L::kQK);
-          if (!SO) {
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-              tma_load_3d(qk_q(s) + b * C * 128, x.tmq, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
-          }
-#pragma unroll
-          for (int b = 0; b < 2; ++b)
-            tma_load_3d(qk_k(s) + b * C * 128, x.tmk, hh * 128 + b * 64, row, bh, bar(L::bQkFull + s));
+          load_qk<L, SO>(sbase, x.tmq, x.tmk, u, hh, row, bh);
           qk_issued = u + 1;
         }
       }
@@ -1244,14 +1261,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   float* pw = reinterpret_cast<float*>(sm + L::oPw);  // pw[d] = gamma^d, d = 0..C
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oSlot);
-  const int head = cta_pos(p).bh % p.H;
-  const float g = p.gamma[head];
-  const float lg = g > 0.f ? log2f(g) : 0.f;
-  const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
   const int warp = threadIdx.x >> 5;
   float inv_gC = 1.f;
 
   // ---- set-up ----
+  // The first chunks' slots are free, so for a split sequence (every CTA in
+  // the first wave, the latency chain of pre-pass and main pass) the producer
+  // thread issues their loads as soon as the barriers exist, before the wait
+  // for gamma, the tables and the TMEM allocation.  Measured: mid -1.5 us,
+  // long -1.5 us; with several waves of unsplit CTAs (7B-shaped) the early
+  // burst cost 2%, so it is off there.
+  const CtaPos pos = cta_pos(p);
+  const int c_begin = pos.seg * p.seg_chunks;
+  const int nck = min(c_begin + p.seg_chunks, p.n_chunks) - c_begin;
+  const int pre = p.segments > 1 ? max(0, min(nck, min(L::NV, L::NQK / L::H))) : 0;
   if (threadIdx.x == 0) {
     init_barriers<C, DK, DVT, SO>(sbase);
     *abort_flag = 0;
@@ -1260,11 +1283,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
     if (!SO) prefetch_tensormap(&tmo);
+    for (int i = 0; i < pre; ++i) {
+      const int row = (c_begin + i) * C;
+      load_v<L, SO>(sbase, &tmv, i, row, pos.dvt * DVT, pos.bh);
+      for (int hh = 0; hh < L::H; ++hh) load_qk<L, SO>(sbase, &tmq, &tmk, i * L::H + hh, hh, row, pos.bh);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
+  const float g = p.gamma[pos.bh % p.H];
+  const float lg = g > 0.f ? log2f(g) : 0.f;
+  const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
   for (int d = threadIdx.x; d <= C; d += blockDim.x) pw[d] = gamma_pow(g, lg, (float)d);
   tc_fence_before();
   __syncthreads();
@@ -1276,7 +1307,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   // grid can never hold the columns this CTA still needs.
   if (SO) griddep_launch_dependents();
 
-  const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC};
+  const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC, pre};
   if (fast) chunk_roles<C, DK, DVT, SO, true, NORM, ROT>(p, x);
   else chunk_roles<C, DK, DVT, SO, false, NORM, ROT>(p, x);
 
