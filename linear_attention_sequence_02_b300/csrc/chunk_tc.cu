@@ -1272,6 +1272,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   // long -1.5 us; with several waves of unsplit CTAs (7B-shaped) the early
   // burst cost 2%, so it is off there.
   const CtaPos pos = cta_pos(p);
+  const float g = p.gamma[pos.bh % p.H];  // issued first: its latency overlaps the set-up
   const int c_begin = pos.seg * p.seg_chunks;
   const int nck = min(c_begin + p.seg_chunks, p.n_chunks) - c_begin;
   const int pre = p.segments > 1 ? max(0, min(nck, min(L::NV, L::NQK / L::H))) : 0;
@@ -1293,7 +1294,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
-  const float g = p.gamma[pos.bh % p.H];
   const float lg = g > 0.f ? log2f(g) : 0.f;
   const bool fast = g > 0.f && (float)C * lg >= kMinChunkDecayLog2;
   for (int d = threadIdx.x; d <= C; d += blockDim.x) pw[d] = gamma_pow(g, lg, (float)d);
