@@ -49,7 +49,10 @@
 //
 // Long sequences are cut into segments so that enough CTAs fill the GPU.  A
 // state-only pre-pass (this kernel with SO = true: K and V only) writes each
-// segment's local end state to a float32 workspace; the main pass starts
+// segment's local end state, sum_m gamma^(Lseg-1-m) k_m^T v_m, to a float32
+// workspace.  It walks the segment from its last chunk back to its first with
+// each chunk's decay in its W, so one accumulating MMA chain serves any gamma
+// (no rescaled state, no direct form).  The main pass starts
 // segment s from gamma^(s Lseg) state_in (the caller's starting state, if any)
 // plus sum_{t<s} gamma^((s-1-t) Lseg) state_t.  The main pass is launched with
 // programmatic stream serialisation: its CTAs start while the pre-pass runs
@@ -476,7 +479,11 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   const float g = p.gamma[head];
   const float lg = g > 0.f ? log2f(g) : 0.f;
   const bool zero_init = SO || (seg == 0 && p.state_in == nullptr);
-  auto chunk_len = [&](int i) { return min(C, p.N - (c_begin + i) * C); };
+  // The state-only pass walks its segment from the last chunk back to the
+  // first (its sum does not depend on the order; the weights then need no
+  // running rescale).  chunk_at(i) is the sequence chunk of the CTA's i-th step.
+  auto chunk_at = [&](int i) { return SO ? c_begin + nck - 1 - i : c_begin + i; };
+  auto chunk_len = [&](int i) { return min(C, p.N - chunk_at(i) * C); };
   // Segment states in the workspace are stored lane-major: float4 number
   // (c4 * 128 + row) of block (bh, segment, dv tile, half) holds columns
   // 4c4..4c4+3 of state row `row`, so a warp's 32 rows are 512 contiguous bytes.
@@ -567,7 +574,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       int v_issued = x.pre, qk_issued = x.pre * H;
       bool ok = true;
       for (int i = x.pre; i < nck && ok; ++i) {
-        const int row = (c_begin + i) * C;
+        const int row = chunk_at(i) * C;
         {
           const int s = i % NV, k = i / NV;
           if (k > 0 && !wait_bar(bar(L::bVEmpty + s), (k - 1) & 1, abort_flag)) {
@@ -648,22 +655,20 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           return true;
         };
         if (SO) {
-          // state only: S in chunk order, each once its W (or K^) and, in the
-          // direct form, the decayed state are ready
+          // state only, last chunk first: S += K^T W with every chunk's decay
+          // in its W (any gamma), one accumulating MMA chain
           RingPos<NV> v;
           RingPos<NQK> qs;
           for (int i = 0; i < nck && ok; ++i) {
-            if (fast) frame_advance(c, n, inv_g(i));
-            if (!wait(bWReady + 8 * v.slot, v.phase) || (!fast && !wait(bVFull + 8 * v.slot, v.phase))) {
+            if (!wait(bWReady + 8 * v.slot, v.phase)) {
               ok = false;
               break;
             }
             for (int hh = 0; hh < H && ok; ++hh) {
-              ok = wait_qk(i * H + hh + 1) && (fast || wait(bSRead + 8 * hh, (uint32_t)i));
+              ok = wait_qk(i * H + hh + 1);
               if (!ok) break;
               tc_fence_after();
-              mma_s(tmem + L::cS + hh * DVT, qs.slot, v.slot, i > 0, n);
-              if (!fast) mma_commit(bSFull + 8 * hh);
+              mma_s(tmem + L::cS + hh * DVT, qs.slot, v.slot, i > 0, 0);
               if (!L::kUnifiedStage) mma_commit(bQkEmpty + 8 * qs.slot);
               qs.next();
             }
@@ -788,14 +793,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     // direct form: K <- diag(gamma^(L-1-m)) K and Q <- diag(scale gamma^(t+1)) Q in place
     auto kq_pass = [&](int i) -> bool {
       const int len = chunk_len(i);
-      if (SO) {
-        for (int hh = 0; hh < H; ++hh) {
-          const int u = i * H + hh;
-          if (!gw((ROT ? L::bQkRot : L::bQkFull) + u % NQK, (u / NQK) & 1)) return false;
-        }
-      } else if (!gw(L::bPFull + i % NP, (i / NP) & 1)) {
-        return false;
-      }
+      if (!gw(L::bPFull + i % NP, (i / NP) & 1)) return false;
       for (int hh = 0; hh < H; ++hh) {
         const int s = (i * H + hh) % NQK;
         scale_rows_bf16<L::kK, C>(sm + s * L::kQK + L::kQ, et,
@@ -885,38 +883,12 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
     int n = 0;
     bool alive = true;
     if (SO) {
-      if (fast) {
-        for (int i = 0; i < nck && alive; ++i) {
-          frame_advance(c, n, inv_g(i));
-          alive = w_pass(i, c);
-        }
-      } else {
-        for (int i = 0; i < nck && alive; ++i) {
-          if (!kq_pass(i)) { alive = false; break; }
-          // decay the carried state by gamma^L (zero before the first chunk)
-          if (i > 0) {
-            const float gL = pw[chunk_len(i)];
-#pragma unroll 1
-            for (int hh = 0; hh < H && alive; ++hh) {
-              if (!gw(L::bSFull + hh, (i - 1) & 1)) { alive = false; break; }
-              tc_fence_after();
-#pragma unroll 1
-              for (int cb = 0; cb < DVT / 32; ++cb) {
-                uint32_t r[32];
-                const uint32_t ta = tmem + lane_addr + L::cS + hh * DVT + cb * 32;
-                tmem_ld32(ta, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gL);
-                tmem_st32(ta, r);
-              }
-            }
-            tmem_wait_st();
-            if (!alive) break;
-          }
-          tc_fence_before();
-          for (int hh = 0; hh < H; ++hh) mbar_arrive(bar(L::bSRead + hh));
-        }
+      // last chunk first: the i-th step's tokens are weighted by gamma to the
+      // number of tokens after them in the segment (c stays 1)
+      float after = 0.f;
+      for (int i = 0; i < nck && alive; ++i) {
+        alive = w_pass(i, gamma_pow(g, lg, after));
+        after += (float)chunk_len(i);
       }
     } else {
       if (fast) {
@@ -987,7 +959,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
             cj[e] = __cosf(a);
           }
           float ca[4], sa[4];
-          const float pos = (float)(p.n0 + (c_begin + i) * C + r0);
+          const float pos = (float)(p.n0 + chunk_at(i) * C + r0);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float a = reduced_angle(pos, tj[e]);
@@ -1285,7 +1257,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     prefetch_tensormap(&tmv);
     if (!SO) prefetch_tensormap(&tmo);
     for (int i = 0; i < pre; ++i) {
-      const int row = (c_begin + i) * C;
+      const int row = (SO ? c_begin + nck - 1 - i : c_begin + i) * C;  // the roles' chunk order
       load_v<L, SO>(sbase, &tmv, i, row, pos.dvt * DVT, pos.bh);
       for (int hh = 0; hh < L::H; ++hh) load_qk<L, SO>(sbase, &tmq, &tmk, i * L::H + hh, hh, row, pos.bh);
     }
