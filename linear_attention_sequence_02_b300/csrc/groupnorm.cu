@@ -144,8 +144,8 @@ cudaError_t launch_groupnorm_bf16(const void* r, const float* weight, const floa
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  if (dv <= 128) return launch_g<1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
-  if (dv <= 256) return launch_g<2, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  if (dv <= 128) return launch_g<1, 8>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  if (dv <= 256) return launch_g<2, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
   if (dv <= 512) return launch_g<4, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
   return launch_g<8, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
 }

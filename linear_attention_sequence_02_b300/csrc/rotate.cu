@@ -30,28 +30,30 @@ namespace ret {
 namespace {
 
 constexpr int kRotThreads = 256;
-constexpr int kRotInFlight = 4;  // (b, h) rows a thread loads before it rotates any
+constexpr int kRotInFlight = 8;  // (b, h) rows a thread loads before it rotates any
 
 __global__ void __launch_bounds__(kRotThreads)
-rotate_kernel(const __nv_bfloat16* x, const float* __restrict__ theta, __nv_bfloat16* y, int BH, int N,
-              int d, int n0, int rows_per_cta) {
+rotate_kernel(const __nv_bfloat16* x, const float* __restrict__ theta, __nv_bfloat16* y, int BH, int N, int d,
+              int n0, int rows_per_cta) {
   const int chunks = d / 8;
   const int t = blockIdx.x * kRotThreads + threadIdx.x;  // token n, chunk c8
   if (t >= N * chunks) return;
   const int n = t / chunks, c8 = t - n * chunks;
-  const float p = (float)(n0 + n);
-  float cs[4], sn[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) sincosf(reduced_angle(p, __ldg(theta + 4 * c8 + e)), &sn[e], &cs[e]);
   const int bh0 = blockIdx.y * rows_per_cta;
   const int bh1 = min(BH, bh0 + rows_per_cta);
   const size_t row = (size_t)N * d;  // elements between (b, h) rows
   const size_t off = (size_t)n * d + 8 * c8;
   for (int bh = bh0; bh < bh1; bh += kRotInFlight) {
+    // the loads first, so their latency overlaps the angles (first batch) or
+    // the previous batch's stores
     uint4 v[kRotInFlight];
 #pragma unroll
     for (int u = 0; u < kRotInFlight; ++u)
       if (bh + u < bh1) v[u] = *reinterpret_cast<const uint4*>(x + (size_t)(bh + u) * row + off);
+    float cs[4], sn[4];
+    const float p = (float)(n0 + n);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sincosf(reduced_angle(p, __ldg(theta + 4 * c8 + e)), &sn[e], &cs[e]);
 #pragma unroll
     for (int u = 0; u < kRotInFlight; ++u) {
       if (bh + u < bh1) {
@@ -80,8 +82,10 @@ cudaError_t launch_rotate_bf16(const void* x, const float* theta, void* y, int B
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long gx = ((long long)N * (d / 8) + kRotThreads - 1) / kRotThreads;
-  // about four CTAs per SM in all: split the (b, h) rows over blockIdx.y
+  // about four CTAs per SM in all: split the (b, h) rows over blockIdx.y, a
+  // multiple of the rows a thread has in flight
   long long rows = (BH * gx + 4LL * sms - 1) / (4LL * sms);
+  rows = (rows + kRotInFlight - 1) / kRotInFlight * kRotInFlight;
   if (rows < 1) rows = 1;
   if (rows > BH) rows = BH;
   const long long gy = (BH + rows - 1) / rows;

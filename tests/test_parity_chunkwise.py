@@ -2,8 +2,8 @@
 against the fp64 oracle: multi-tile cases with ragged tails over every
 compiled (chunk, d_k, value-tile) variant, the segment-split path, guard
 bands around the outputs, continuation into the decode step, and the three
-bf16 workloads at full size (mid and 7B-shaped on sampled heads and rows,
-long-context on sampled heads)."""
+bf16 workloads at full size (mid and long-context on every head, 7B-shaped on
+two whole batch rows and sampled rows of every other head)."""
 import numpy as np
 import pytest
 import torch
@@ -185,20 +185,29 @@ def _sampled_heads_check(orc, q, k, v, g, out, st, C, heads, rows_per_other=6, r
             assert_close(out[b, h, rows], ref, TOL_BF16, f"rows ({b},{h})", per_head=False)
 
 
-def test_long_context_workload_sampled(orc):
-    """B=1, H=16, N=16384, d_k=128, d_v=256, chunk=128."""
+def test_long_context_workload_full(orc):
+    """B=1, H=16, N=16384, d_k=128, d_v=256, chunk=128: every output and state
+    of every head against the oracle's chunkwise form."""
     B, H, N, dk, dv, C = 1, 16, 16384, 128, 256, 128
     q, k, v = inputs.qkv(B, H, N, dk, dv, 0, torch.bfloat16)
     g = gammas(H)
     out, st = run_chunkwise(q, k, v, g, C)
-    _sampled_heads_check(orc, q, k, v, g, out, st, C, heads=[(0, 0), (0, 7), (0, 15)])
+    ref_out, ref_state = orc.chunkwise(q, k, v, g.double(), C)
+    assert_close(out, ref_out, TOL_BF16, "long out")
+    assert_close(st, ref_state, TOL_BF16, "long state")
 
 
-def test_7b_shaped_workload_sampled(orc):
-    """B=8, H=16, N=8192, d_k=256, d_v=512, chunk=128."""
+def test_7b_shaped_workload(orc):
+    """B=8, H=16, N=8192, d_k=256, d_v=512, chunk=128: batch rows 0 and 7 in
+    full (all 16 heads, every token and state), and rows of every other head
+    against the parallel-form definition."""
     B, H, N, dk, dv, C = 8, 16, 8192, 256, 512, 128
     q, k, v = inputs.qkv(B, H, N, dk, dv, 0, torch.bfloat16)
     g = gammas(H)
     out, st = run_chunkwise(q, k, v, g, C)
-    _sampled_heads_check(orc, q, k, v, g, out, st, C, heads=[(0, 0), (3, 9), (7, 15)],
-                         rows_per_other=3)
+    for b in (0, B - 1):
+        sl = slice(b, b + 1)
+        ref_o, ref_s = orc.chunkwise(q[sl], k[sl], v[sl], g.double(), C)
+        assert_close(out[sl], ref_o, TOL_BF16, f"7B out, batch row {b}")
+        assert_close(st[sl], ref_s, TOL_BF16, f"7B state, batch row {b}")
+    _sampled_heads_check(orc, q, k, v, g, out, st, C, heads=[], rows_per_other=3)
