@@ -104,14 +104,19 @@ def decode_bytes(w) -> int:
     return B * H * (8 * dk * dv + 2 * (2 * dk + dv) + 2 * dv)
 
 
-# The source file of the kernel each workload's traffic was captured on.
-TRAFFIC_SOURCE = {"decode_step": "simt.cu", "groupnorm": "groupnorm.cu", "rotate": "rotate.cu"}
+# The source files of the kernels each workload's traffic was captured on.
+TRAFFIC_SOURCE = {"decode_step": ("simt.cu",), "groupnorm": ("groupnorm.cu",), "rotate": ("rotate.cu",),
+                  "mid_parallel": ("parallel_tc.cu",), "long_parallel": ("parallel_tc.cu",),
+                  "mid_backward": ("bwd_tc.cu", "chunk_tc.cu")}
 
 
 def kernel_sha(workload: str = "mid") -> str:
-    name = TRAFFIC_SOURCE.get(workload, "chunk_tc.cu")
-    path = os.path.join(ROOT, "linear_attention_sequence_02_b300", "csrc", name)
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    """sha256[:16] of the kernel source (of the concatenated sources where a call runs kernels of several files)."""
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCE.get(workload, ("chunk_tc.cu",)):
+        with open(os.path.join(ROOT, "linear_attention_sequence_02_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):

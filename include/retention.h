@@ -89,9 +89,12 @@ typedef enum {
  * rounding order); chunk 32 runs on 64-token tiles, the tensor cores'
  * smallest tile height.  Widths below the kernel's tile (128 or 256 query
  * and key columns, 64 or 128 value columns) are padded with zeros by the
- * loads, which leaves every product unchanged.  When the
- * call splits the sequence into segments to fill the GPU it allocates a
- * float32 scratch buffer stream-ordered (cudaMallocAsync / cudaFreeAsync on
+ * loads, which leaves every product unchanged.  The work is cut into units,
+ * one per (batch row, head, value tile).  With fewer units than SMs every
+ * unit's sequence is split into segments; with more, only the units of the
+ * last, partial wave are split (so that wave holds about one CTA per SM).
+ * When the call splits sequences it allocates a float32 scratch buffer for
+ * the segment states stream-ordered (cudaMallocAsync / cudaFreeAsync on
  * `stream`); retention_chunkwise_ws takes a caller-provided buffer instead.
  */
 int retention_chunkwise(const void *q, const void *k, const void *v, const float *gamma,
@@ -229,9 +232,13 @@ int retention_chunkwise_workspace_size(int B, int H, int N, int dk, int dv, int 
 
 /*
  * retention_chunkwise_ws -- retention_chunkwise with caller-owned scratch:
- * `workspace` is a device buffer of at least `workspace_bytes` bytes (as given
- * by retention_chunkwise_workspace_size; may be NULL when that is 0), 256-byte
+ * `workspace` is a device buffer of `workspace_bytes` bytes, 256-byte
  * aligned, used only by the work this call enqueues.  No memory is allocated.
+ * retention_chunkwise_workspace_size gives the size of the preferred plan.
+ * With less, a call whose last partial wave would be split runs those units
+ * whole instead (same results; that wave takes longer); a call that needs
+ * the scratch for every unit (fewer units than SMs) and gets less returns
+ * RET_ERR_INVALID.  `workspace` may be NULL with workspace_bytes 0.
  */
 int retention_chunkwise_ws(const void *q, const void *k, const void *v, const float *gamma,
                            void *out, float *state_out,
@@ -249,9 +256,12 @@ int retention_chunkwise_ws(const void *q, const void *k, const void *v, const fl
  *
  * Scratch: the segment states live in a file-scope device array of
  * 8 MiB (8388608 bytes) that every GPU loading the library reserves until the
- * process exits.  Shapes whose plan needs more scratch than that (see
- * retention_chunkwise_workspace_size) return RET_ERR_UNSUPPORTED before
- * anything is enqueued.  Nothing in the array has to start at zero: each call
+ * process exits.  The call runs the plan retention_chunkwise_ws runs with
+ * 8 MiB of workspace: where retention_chunkwise would cut the units of a last,
+ * partial wave (see retention_chunkwise_ws) and their states need more, those
+ * units run whole instead.  Shapes whose plan needs more scratch than that
+ * even so (fewer units than SMs, every unit cut) return RET_ERR_UNSUPPORTED
+ * before anything is enqueued.  Nothing in the array has to start at zero: each call
  * writes every slot it later reads, so stale contents of an earlier call are
  * never used.
  * Set-up: the first call on a device, with that device current, looks up the

@@ -67,10 +67,13 @@ int num_sms() {
   return n;
 }
 
-// The bf16 chunkwise plan for these sizes, or an error status.
-int plan_chunkwise(int B, int H, int N, int dk, int dv, int chunk, int sms, ret::ChunkPlan* plan) {
+// The bf16 chunkwise plan for these sizes, or an error status.  ws_limit:
+// the workspace the caller can give (the last wave's units are cut only if
+// their segment states fit).
+int plan_chunkwise(int B, int H, int N, int dk, int dv, int chunk, int sms, ret::ChunkPlan* plan,
+                   size_t ws_limit = SIZE_MAX) {
   if (B <= 0 || H <= 0 || N < 0 || dk <= 0 || dv <= 0 || chunk <= 0) return RET_ERR_INVALID;
-  if (!ret::chunk_tc_plan(B, H, N, dk, dv, chunk, sms, plan)) return RET_ERR_UNSUPPORTED;
+  if (!ret::chunk_tc_plan(B, H, N, dk, dv, chunk, sms, plan, ws_limit)) return RET_ERR_UNSUPPORTED;
   return RET_OK;
 }
 
@@ -158,6 +161,20 @@ int backward_call(bool bf16, const void* q, const void* k, const void* v, const 
 
 }  // namespace
 
+namespace ret {
+// Workspace of the plan a call with at most `limit` bytes of workspace runs.
+int chunkwise_workspace_within(int B, int H, int N, int dk, int dv, int chunk, size_t limit, size_t* bytes) {
+  if (!bytes) return RET_ERR_INVALID;
+  ChunkPlan plan;
+  const int sms = num_sms();
+  if (sms <= 0) return RET_ERR_CUDA;
+  const int st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan, limit);
+  if (st != RET_OK) return st;
+  *bytes = plan.workspace_bytes;
+  return RET_OK;
+}
+}  // namespace ret
+
 extern "C" {
 
 int retention_version(void) { return 100; }
@@ -227,7 +244,7 @@ int retention_chunkwise_ws(const void* q, const void* k, const void* v, const fl
   ret::ChunkPlan plan;
   const int sms = num_sms();
   if (sms <= 0) return RET_ERR_CUDA;
-  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
+  st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan, workspace ? workspace_bytes : 0);
   if (st != RET_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) return zero_state(state_out, B, H, dk, dv, s);

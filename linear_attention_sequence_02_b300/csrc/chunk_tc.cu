@@ -48,6 +48,9 @@
 // Warp w (w >= 2) reads TMEM lanes 32*(w%4) .. +31.
 //
 // Long sequences are cut into segments so that enough CTAs fill the GPU.  A
+// unit is one (head, value tile); when there are more units than SMs, only
+// the units of the last, partial wave are cut (so that wave holds as many
+// shorter CTAs as there are SMs), and the others run whole.  A
 // state-only pre-pass (this kernel with SO = true: K and V only) writes each
 // segment's local end state, sum_m gamma^(Lseg-1-m) k_m^T v_m, to a float32
 // workspace.  It walks the segment from its last chunk back to its first with
@@ -195,6 +198,7 @@ struct TcParams {
   const float* norm_b;  //   (null: one, zero) and eps
   float norm_eps;
   int H, N, dv, n_dv_tiles, BH, segments, seg_chunks, n_chunks;
+  int full_units;    // leading units (b*H+h)*n_dv_tiles + tile run whole; the others in `segments`
   int dk;            // query/key width (<= DK; the columns past it are zero-filled by the loads)
   float scale;       // factor of the query (1/sqrt(dk) unless the caller sets another)
   unsigned int test_stall_us;  // > 0: failure-path test (see retention_test_stall_waits)
@@ -202,16 +206,32 @@ struct TcParams {
   int n0;              //   and the position of token 0
 };
 
-// Position of this CTA: value tile, head (b*H+h) and sequence segment, value
-// tile fastest, then head, then segment.
+// Position of this CTA.  Units u = (b*H+h) * n_dv_tiles + value tile.  The
+// main pass runs units 0 .. full_units-1 whole (CTA u), then the cut units
+// segment by segment (segment 0 of each, then segment 1, ...); the pre-pass
+// runs segments 0 .. segments-2 of the cut units in the same order.
 struct CtaPos {
   int dvt, bh, seg;
+  int nseg;        // segments of this unit (1: whole)
+  int seg_chunks;  // chunks per segment of this unit
+  int cut;         // index of the unit among the cut ones (workspace block), -1 if whole
 };
+template <bool SO>
 __device__ __forceinline__ CtaPos cta_pos(const TcParams& p) {
-  int idx = blockIdx.x;
-  const int dvt = idx % p.n_dv_tiles;
-  idx /= p.n_dv_tiles;
-  return CtaPos{dvt, idx % p.BH, idx / p.BH};
+  const int x = blockIdx.x;
+  int u, seg = 0, cut = -1;
+  if (!SO && x < p.full_units) {
+    u = x;
+  } else {
+    const int n_cut = p.BH * p.n_dv_tiles - p.full_units;
+    const int y = SO ? x : x - p.full_units;
+    cut = y % n_cut;
+    seg = y / n_cut;
+    u = p.full_units + cut;
+  }
+  const bool whole = cut < 0;
+  return CtaPos{u % p.n_dv_tiles, u / p.n_dv_tiles, seg, whole ? 1 : p.segments,
+                whole ? p.n_chunks : p.seg_chunks, cut};
 }
 
 __device__ __forceinline__ float gamma_pow(float g, float lg, float d) {
@@ -369,10 +389,10 @@ template <int C, int DK, int DVT, bool SO>
 __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, uint32_t tmem) {
   using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H;
-  const CtaPos pos = cta_pos(p);
+  const CtaPos pos = cta_pos<SO>(p);
   const int dvt = pos.dvt, bh = pos.bh, seg = pos.seg;
-  const int nck = min(seg * p.seg_chunks + p.seg_chunks, p.n_chunks) - seg * p.seg_chunks;
-  const bool to_out = !SO && seg == p.segments - 1 && p.state_out != nullptr;
+  const int nck = min(seg * pos.seg_chunks + pos.seg_chunks, p.n_chunks) - seg * pos.seg_chunks;
+  const bool to_out = !SO && seg == pos.nseg - 1 && p.state_out != nullptr;
   if (!(SO || to_out) || nck <= 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dv0 = dvt * DVT;
@@ -391,9 +411,9 @@ __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, u
         float4* dst;
         size_t stride;
         if (SO) {
-          // float4 number (c4 * 128 + row) of block (bh, segment, dv tile, half)
+          // float4 number (c4 * 128 + row) of block (cut unit, segment, half)
           dst = reinterpret_cast<float4*>(p.ws) +
-                ((((size_t)bh * (p.segments - 1) + seg) * p.n_dv_tiles + dvt) * H + hh) * (size_t)(DVT / 4) * 128 +
+                (((size_t)pos.cut * (p.segments - 1) + seg) * H + hh) * (size_t)(DVT / 4) * 128 +
                 (size_t)(cb * 8) * 128 + srow;
           stride = 128;
         } else {
@@ -473,11 +493,11 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   auto qk_k = [&](int s) { return sbase + s * L::kQK + L::kQ; };
   auto v_slot = [&](int s) { return sbase + L::oV + s * L::kV; };
   auto sb_buf = [&](int b) { return sbase + L::oSb + b * L::kSb; };
-  const CtaPos pos = cta_pos(p);
+  const CtaPos pos = cta_pos<SO>(p);
   const int dvt = pos.dvt, bh = pos.bh, seg = pos.seg;
   const int head = bh % p.H;
-  const int c_begin = seg * p.seg_chunks;
-  const int nck = min(c_begin + p.seg_chunks, p.n_chunks) - c_begin;
+  const int c_begin = seg * pos.seg_chunks;
+  const int nck = min(c_begin + pos.seg_chunks, p.n_chunks) - c_begin;
   const int dv0 = dvt * DVT;
   const float g = p.gamma[head];
   const float lg = g > 0.f ? log2f(g) : 0.f;
@@ -488,11 +508,10 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   auto chunk_at = [&](int i) { return SO ? c_begin + nck - 1 - i : c_begin + i; };
   auto chunk_len = [&](int i) { return min(C, p.N - chunk_at(i) * C); };
   // Segment states in the workspace are stored lane-major: float4 number
-  // (c4 * 128 + row) of block (bh, segment, dv tile, half) holds columns
+  // (c4 * 128 + row) of block (cut unit, segment, half) holds columns
   // 4c4..4c4+3 of state row `row`, so a warp's 32 rows are 512 contiguous bytes.
   auto ws_block = [&](int s, int hh) {
-    return reinterpret_cast<float4*>(p.ws) +
-           ((((size_t)bh * (p.segments - 1) + s) * p.n_dv_tiles + dvt) * H + hh) * (size_t)(DVT / 4) * 128;
+    return reinterpret_cast<float4*>(p.ws) + (((size_t)pos.cut * (p.segments - 1) + s) * H + hh) * (size_t)(DVT / 4) * 128;
   };
   auto inv_g = [&](int i) {
     const int len = chunk_len(i);
@@ -508,7 +527,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   // flight), then meet at a barrier of both groups.
   auto init_state = [&](int srow, uint32_t lane_addr, int cb0, int cb1) {
     if (seg > 0) griddep_wait();  // the pre-pass wrote the workspace
-    const float seg_len = (float)p.seg_chunks * (float)C;
+    const float seg_len = (float)pos.seg_chunks * (float)C;
 #pragma unroll 1
     for (int hh = 0; hh < H; ++hh) {
 #pragma unroll 1
@@ -1246,11 +1265,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   // for gamma, the tables and the TMEM allocation.  Measured: mid -1.5 us,
   // long -1.5 us; with several waves of unsplit CTAs (7B-shaped) the early
   // burst cost 2%, so it is off there.
-  const CtaPos pos = cta_pos(p);
+  const CtaPos pos = cta_pos<SO>(p);
   const float g = p.gamma[pos.bh % p.H];  // issued first: its latency overlaps the set-up
-  const int c_begin = pos.seg * p.seg_chunks;
-  const int nck = min(c_begin + p.seg_chunks, p.n_chunks) - c_begin;
-  const int pre = p.segments > 1 ? max(0, min(nck, min(L::NV, L::NQK / L::H))) : 0;
+  const int c_begin = pos.seg * pos.seg_chunks;
+  const int nck = min(c_begin + pos.seg_chunks, p.n_chunks) - c_begin;
+  const int pre = pos.nseg > 1 ? max(0, min(nck, min(L::NV, L::NQK / L::H))) : 0;
   if (threadIdx.x == 0) {
     init_barriers<C, DK, DVT, SO>(sbase);
     *abort_flag = 0;
@@ -1392,12 +1411,12 @@ template <int C, int DK, int DVT, bool NORM, bool ROT>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   const bool split = p.segments > 1;
+  const int n_cut = p.BH * p.n_dv_tiles - p.full_units;
   if (split) {
-    cudaError_t e = launch_one<C, DK, DVT, true, false, ROT>(mq, mk, mv, mo, p,
-                                                             p.BH * (p.segments - 1) * p.n_dv_tiles, false, s);
+    cudaError_t e = launch_one<C, DK, DVT, true, false, ROT>(mq, mk, mv, mo, p, n_cut * (p.segments - 1), false, s);
     if (e != cudaSuccess) return e;
   }
-  return launch_one<C, DK, DVT, false, NORM, ROT>(mq, mk, mv, mo, p, p.BH * p.segments * p.n_dv_tiles, split, s);
+  return launch_one<C, DK, DVT, false, NORM, ROT>(mq, mk, mv, mo, p, p.full_units + n_cut * p.segments, split, s);
 }
 
 // The variant for these tile sizes.
@@ -1444,7 +1463,8 @@ std::atomic<unsigned int> g_test_stall_us{0};
 
 int chunk_tc_launch_count(const ChunkPlan& plan) { return plan.launches; }
 
-bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan) {
+bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan,
+                   size_t ws_limit) {
   // chunk 32 runs on 64-token tiles: the chunk length is a tiling choice that
   // leaves the result unchanged (every chunk length computes the same sums),
   // and the tensor cores' smallest tile has 64 rows.
@@ -1460,20 +1480,35 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   plan->n_chunks = (N + plan->chunk - 1) / plan->chunk;
   const long long units = (long long)B * H * plan->n_dv_tiles;
   if (units > (1LL << 30)) return false;
-  // Enough segments that every SM gets a CTA, each segment at least 4 chunks.
+  // Enough segments that every SM gets a CTA, each segment at least 4 chunks:
+  // with fewer units than SMs every unit is cut; with more, the units of the
+  // last, partial wave are cut so that it holds about as many CTAs as there
+  // are SMs (the other units run whole), if their segment states fit within
+  // ws_limit bytes.
+  long long cut = units;
   int segs = 1;
-  if (num_sms > 0 && units < num_sms) segs = (int)(num_sms / units);
+  if (num_sms > 0 && units < num_sms) {
+    segs = (int)(num_sms / units);
+  } else if (num_sms > 0 && units % num_sms != 0) {
+    cut = units % num_sms;
+    segs = (int)(num_sms / cut);
+  }
   segs = std::max(1, std::min(segs, plan->n_chunks / 4));
   int seg_chunks = plan->n_chunks > 0 ? (plan->n_chunks + segs - 1) / segs : 1;
   if (plan->n_chunks > 0) segs = (plan->n_chunks + seg_chunks - 1) / seg_chunks;  // no empty segment
-  plan->segments = std::max(1, segs);
+  // segment states cover the padded tile (dk_tile rows, dvt columns) of each cut unit
+  const size_t ws = segs > 1 ? sizeof(float) * (size_t)cut * (segs - 1) * plan->dk_tile * (size_t)dvt : 0;
+  if (segs <= 1 || (cut < units && ws > ws_limit)) {
+    segs = 1;
+    seg_chunks = std::max(1, plan->n_chunks);
+    cut = units;
+  }
+  plan->segments = segs;
   plan->seg_chunks = std::max(1, seg_chunks);
-  // segment states cover the padded tile (dk_tile rows, n_dv_tiles * dvt columns)
-  plan->workspace_bytes = plan->segments > 1 ? sizeof(float) * (size_t)B * H * (plan->segments - 1) *
-                                                   plan->dk_tile * (size_t)plan->n_dv_tiles * dvt
-                                             : 0;
-  plan->launches = plan->segments > 1 ? 2 : 1;
-  if ((long long)units * plan->segments > INT32_MAX) return false;
+  plan->full_units = segs > 1 ? (int)(units - cut) : (int)units;
+  plan->workspace_bytes = segs > 1 ? ws : 0;
+  plan->launches = segs > 1 ? 2 : 1;
+  if (plan->full_units + cut * segs > INT32_MAX) return false;
   return true;
 }
 
@@ -1508,6 +1543,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.segments = plan.segments;
   p.seg_chunks = plan.seg_chunks;
   p.n_chunks = plan.n_chunks;
+  p.full_units = plan.full_units;
   p.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)dk));
   p.test_stall_us = g_test_stall_us.load(std::memory_order_relaxed);
   p.theta = rot ? rot->theta : nullptr;

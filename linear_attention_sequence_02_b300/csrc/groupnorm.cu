@@ -11,10 +11,13 @@
 //
 // R is the retention output layout [B][H][N][dv] (bf16); Y is written with the
 // heads concatenated per token, [B][N][H][dv] (bf16), the layout the output
-// projection reads.  A warp takes R consecutive rows of one (b, h) at a time:
-// coalesced reads of all R rows first (so R dv bf16 are in flight), then per row
-// two warp-shuffle reductions (mean, then the centred second moment) in fp32
-// and a coalesced write.  The kernel is bound by HBM: 4 dv bytes per row.
+// projection reads.  A warp takes a batch of consecutive rows of one (b, h):
+// coalesced reads of the whole batch first, then per row two shuffle
+// reductions (mean, then the centred second moment) in fp32 and a coalesced
+// write.  When dv is a multiple of 8 a row is held by LPR lanes of 8 channels
+// each (16-byte loads and stores; 32 / LPR rows per warp instruction, and the
+// reductions of a batch's rows interleaved); otherwise a row is held by the
+// whole warp, 4 channels a lane.  Bound by HBM: 4 dv bytes per row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -119,13 +122,139 @@ groupnorm_kernel(const __nv_bfloat16* __restrict__ r, const float* __restrict__ 
   }
 }
 
+// Rows of a multiple of 8 channels: LPR lanes (a power of two, <= 32) hold one
+// row, 8 channels 8 (li + LPR g) + e a lane for g < G; a warp covers 32 / LPR
+// consecutive rows per load instruction and R such groups per batch.  The
+// xor shuffles with offsets below LPR stay inside a row's aligned lane group.
+template <int LPR, int G, int R>
+__global__ void __launch_bounds__(kGnWarps * 32)
+groupnorm_vec_kernel(const __nv_bfloat16* __restrict__ r, const float* __restrict__ weight,
+                     const float* __restrict__ bias, __nv_bfloat16* __restrict__ y, int H, int N, int dv,
+                     float eps) {
+  constexpr int kSlots = 32 / LPR, kRows = kSlots * R;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = lane / LPR, li = lane % LPR;
+  const int bh = blockIdx.y, h = bh % H, b = bh / H;
+  const int n8 = dv / 8;
+  const float inv_dv = 1.f / (float)dv;
+  float wv[G][8], bv[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int c8 = li + LPR * g;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int c = h * dv + 8 * c8 + e;
+      const bool in = c8 < n8;
+      wv[g][e] = (in && weight) ? __ldg(weight + c) : 1.f;
+      bv[g][e] = (in && bias) ? __ldg(bias + c) : 0.f;
+    }
+  }
+  const __nv_bfloat16* rb = r + (size_t)bh * N * dv;     // r[b][h][n][:] = rb + n dv
+  __nv_bfloat16* yb = y + ((size_t)b * N * H + h) * dv;  // y[b][n][h][:] = yb + n H dv
+  const size_t ys = (size_t)H * dv;
+  for (int n0 = (blockIdx.x * kGnWarps + warp) * kRows; n0 < N; n0 += gridDim.x * kGnWarps * kRows) {
+    float x[R][G][8];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int n = n0 + j * kSlots + slot;
+      const uint4* src = reinterpret_cast<const uint4*>(rb + (size_t)n * dv);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int c8 = li + LPR * g;
+        if (n < N && c8 < n8) {
+          const uint4 u = __ldg(src + c8);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+            x[j][g][2 * e] = f.x;
+            x[j][g][2 * e + 1] = f.y;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[j][g][e] = 0.f;
+        }
+      }
+    }
+    float t[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      float a = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) a += x[j][g][e] + x[j][g][e + 1];
+      t[j] = a;
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < R; ++j) t[j] += __shfl_xor_sync(0xffffffffu, t[j], o);
+    float mu[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      mu[j] = t[j] * inv_dv;
+      float q = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (li + LPR * g < n8) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float d = x[j][g][e] - mu[j];
+            q = fmaf(d, d, q);
+          }
+        }
+      }
+      t[j] = q;
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < R; ++j) t[j] += __shfl_xor_sync(0xffffffffu, t[j], o);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int n = n0 + j * kSlots + slot;
+      const float inv = rsqrtf(t[j] * inv_dv + eps);
+      uint4* dst = reinterpret_cast<uint4*>(yb + (size_t)n * ys);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int c8 = li + LPR * g;
+        if (n < N && c8 < n8) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 o2 = __floats2bfloat162_rn(fmaf((x[j][g][2 * e] - mu[j]) * inv, wv[g][2 * e], bv[g][2 * e]),
+                                                            fmaf((x[j][g][2 * e + 1] - mu[j]) * inv, wv[g][2 * e + 1],
+                                                                 bv[g][2 * e + 1]));
+            w4[e] = *reinterpret_cast<const uint32_t*>(&o2);
+          }
+          dst[c8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+    }
+  }
+}
+
+// about eight CTAs per SM in all, at least one row batch per CTA
+inline int gn_grid_x(int B, int H, int N, int rows_per_cta, int sms) {
+  const int per_bh = (N + rows_per_cta - 1) / rows_per_cta;
+  const long long want_x = ((long long)sms * 8 + (long long)B * H - 1) / ((long long)B * H);
+  return (int)(want_x < per_bh ? (want_x < 1 ? 1 : want_x) : per_bh);
+}
+
+template <int LPR, int G, int R>
+cudaError_t launch_vec(const void* r, const float* weight, const float* bias, void* y, int B, int H, int N,
+                       int dv, float eps, int sms, cudaStream_t s) {
+  const int gx = gn_grid_x(B, H, N, kGnWarps * (32 / LPR) * R, sms);
+  groupnorm_vec_kernel<LPR, G, R><<<dim3(gx, B * H), kGnWarps * 32, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(r), weight, bias, static_cast<__nv_bfloat16*>(y), H, N, dv, eps);
+  return cudaGetLastError();
+}
+
 template <int G, int R>
 cudaError_t launch_g(const void* r, const float* weight, const float* bias, void* y, int B, int H, int N,
                      int dv, float eps, int sms, cudaStream_t s) {
-  // about eight CTAs per SM in all, at least one row block per CTA
-  const int per_bh = (N + kGnWarps * R - 1) / (kGnWarps * R);
-  const long long want_x = ((long long)sms * 8 + (long long)B * H - 1) / ((long long)B * H);
-  const int gx = (int)(want_x < per_bh ? (want_x < 1 ? 1 : want_x) : per_bh);
+  const int gx = gn_grid_x(B, H, N, kGnWarps * R, sms);
   groupnorm_kernel<G, R><<<dim3(gx, B * H), kGnWarps * 32, 0, s>>>(
       static_cast<const __nv_bfloat16*>(r), weight, bias, static_cast<__nv_bfloat16*>(y), H, N, dv, eps);
   return cudaGetLastError();
@@ -144,8 +273,18 @@ cudaError_t launch_groupnorm_bf16(const void* r, const float* weight, const floa
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  if (dv <= 128) return launch_g<1, 8>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
-  if (dv <= 256) return launch_g<2, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  // rows start on 16-byte boundaries when dv is a multiple of 8
+  const bool a16 = dv % 8 == 0 && reinterpret_cast<uintptr_t>(r) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0;
+  if (a16) {
+    if (dv <= 32) return launch_vec<4, 1, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+    if (dv <= 64) return launch_vec<8, 1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+    if (dv <= 128) return launch_vec<16, 1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+    if (dv <= 256) return launch_vec<32, 1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+    if (dv <= 512) return launch_vec<32, 2, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+    return launch_vec<32, 4, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  }
+  if (dv <= 128) return launch_g<1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+  if (dv <= 256) return launch_g<2, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
   if (dv <= 512) return launch_g<4, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
   return launch_g<8, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
 }

@@ -42,14 +42,22 @@ struct ChunkPlan {
   int dk_tile;      // query/key columns the kernel is built for (128 or 256; dk <= dk_tile)
   int dvt;          // value columns per CTA (64 or 128)
   int n_dv_tiles;   // ceil(dv / dvt); the last tile's columns past dv are padding
-  int segments;     // sequence segments per head (>= 1)
+  int segments;     // sequence segments of each cut unit (>= 1; 1: nothing is cut)
   int seg_chunks;   // chunks per segment (all segments but the last are full)
+  int full_units;   // units ((b*H+h) * n_dv_tiles + value tile) run whole; the rest are cut
   int n_chunks;     // ceil(N / chunk)
-  size_t workspace_bytes;  // float32 segment states, 0 if segments == 1
+  size_t workspace_bytes;  // float32 segment states of the cut units, 0 if segments == 1
   int launches;     // kernels enqueued by one call
 };
 // Fills `plan` for a supported shape; returns false for unsupported shapes.
-bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan);
+// When there are more units than SMs, the units of the last, partial wave are
+// cut into segments only if their segment states take at most ws_limit bytes
+// (otherwise every unit runs whole and no workspace is needed).
+bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan,
+                   size_t ws_limit = SIZE_MAX);
+// Workspace bytes of the plan that retention_chunkwise_ws runs when given at
+// most `limit` bytes (a RET_* status; plans on the current device).
+int chunkwise_workspace_within(int B, int H, int N, int dk, int dv, int chunk, size_t limit, size_t* bytes);
 // Kernels a call with this plan enqueues (2 when the sequence is split:
 // state-only pre-pass, then main pass).
 int chunk_tc_launch_count(const ChunkPlan& plan);

@@ -15,6 +15,7 @@
 #include <cstddef>
 #include <mutex>
 
+#include "internal.h"
 #include "retention.h"
 
 namespace {
@@ -49,8 +50,10 @@ cudaError_t static_scratch(int dev, void** ptr) {
 extern "C" int retention_chunkwise_noalloc(const void* q, const void* k, const void* v,
                                            const float* gamma, void* out, float* state_out, int B,
                                            int H, int N, int dk, int dv, int chunk, void* stream) {
+  // the plan that fits the static scratch (a call with more units than SMs
+  // then leaves its last wave whole rather than need more)
   size_t need = 0;
-  int st = retention_chunkwise_workspace_size(B, H, N, dk, dv, chunk, &need);
+  int st = ret::chunkwise_workspace_within(B, H, N, dk, dv, chunk, kStaticScratchBytes, &need);
   if (st != RET_OK) return st;
   if (need > kStaticScratchBytes) return RET_ERR_UNSUPPORTED;  // beyond the static scratch
   int dev = 0;

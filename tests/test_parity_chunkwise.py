@@ -137,6 +137,45 @@ def test_workspace_variant_matches():
         binding.retention_chunkwise_ws(q, k, v, g, C, ws[: nbytes // 2])
 
 
+def test_last_wave_split(orc):
+    """More (head, value tile) units than SMs, not a whole number of waves: the
+    units of the last wave are cut into segments (state-only pre-pass, then
+    the main pass), the others run whole.  The same call with no workspace
+    runs every unit whole; with a starting state; and through the static
+    scratch entry point."""
+    B, H, N, dk, dv, C = 2, 80, 3072, 64, 64, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = B * H
+    q, k, v = inputs.qkv(B, H, N, dk, dv, 5, torch.bfloat16)
+    gen = torch.Generator().manual_seed(5)
+    g = 0.8 + 0.2 * torch.rand(H, generator=gen)
+    g[0], g[1], g[2] = 0.0, 1.0, 0.5
+    if units > sms and units % sms and sms // (units % sms) >= 2:
+        assert binding.chunkwise_launches(B, H, N, dk, dv, C) == 2
+        assert binding.chunkwise_workspace_size(B, H, N, dk, dv, C) > 0
+    ref_out, ref_state = orc.chunkwise(q, k, v, g.double(), C)
+    out, st = run_chunkwise(q, k, v, g, C)
+    assert_close(out, ref_out, TOL_BF16, "last-wave split out")
+    assert_close(st, ref_state, TOL_BF16, "last-wave split state")
+    qd, kd, vd, gd = q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV)
+    o2, s2 = binding.retention_chunkwise_ws(qd, kd, vd, gd, C, None)
+    o3, s3 = binding.retention_chunkwise_noalloc(qd, kd, vd, gd, C)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert_close(o2.cpu(), ref_out, TOL_BF16, "every unit whole, out")
+    assert_close(s2.cpu(), ref_state, TOL_BF16, "every unit whole, state")
+    assert torch.equal(o3.cpu(), out) and torch.equal(s3.cpu(), st)
+    # continued from a state: the prefix's state feeds the rest of the sequence
+    cut = 1024
+    _, s_pre = binding.retention_chunkwise(qd[:, :, :cut].contiguous(), kd[:, :, :cut].contiguous(),
+                                           vd[:, :, :cut].contiguous(), gd, C)
+    o4, s4 = binding.retention_chunkwise_from_state(qd[:, :, cut:].contiguous(), kd[:, :, cut:].contiguous(),
+                                                    vd[:, :, cut:].contiguous(), gd, C, s_pre)
+    torch.cuda.synchronize()
+    assert_close(o4.cpu(), ref_out[:, :, cut:], TOL_BF16, "continued out")
+    assert_close(s4.cpu(), ref_state, TOL_BF16, "continued state")
+
+
 def test_chunkwise_then_decode_continuation(orc):
     """state_out of a prefix, advanced by retention_step, reproduces the whole sequence."""
     B, H, N, dk, dv, C, cut = 1, 4, 200, 128, 256, 64, 160

@@ -29,7 +29,10 @@ def _rows(B, H, N, dv, seed):
 
 
 @pytest.mark.parametrize("B,H,N,dv", [
-    (1, 3, 77, 64),     # half the lanes idle
+    (1, 3, 77, 24),     # 4 lanes a row, the last lane partly idle
+    (1, 3, 77, 64),     # 8 lanes a row
+    (1, 2, 41, 100),    # not a multiple of 8: a warp a row, 4 channels a lane
+    (2, 1, 19, 36),     # not a multiple of 8, most lanes idle
     (2, 2, 33, 192),    # two groups per lane, the second partly idle
     (1, 2, 50, 256),
     (1, 16, 5, 512),
