@@ -366,9 +366,15 @@ int retention_step_rotated(const void *q, const void *k, const void *v, const fl
  * operands (dq the forward of (dout, v, k) from S0^T; dk and dv the
  * time-reversed forwards of (v, dout, q) and (k, q, dout) from dstate^T/(s g)
  * and dstate/(s g); dS0 = s g times the final state of the latter), with bf16
- * operands and float32 accumulation and state, and a stream-ordered scratch
- * buffer (cudaMallocAsync / cudaFreeAsync on `stream`) for the permuted
- * operands.  Otherwise (other widths, or the float32 twin) float32 arithmetic
+ * operands and float32 accumulation and state.  The forwards read q, k, v
+ * and dout in place and write the gradients in place (the time-reversed ones
+ * take the rows from the last to the first); a stream-ordered scratch buffer
+ * (cudaMallocAsync / cudaFreeAsync on `stream`) holds the starting states
+ * and segment states.  The three forwards run concurrently on `stream` and
+ * two streams the library creates per device on its first gradient call
+ * (forked from and joined back to `stream` with events, so the call is
+ * ordered on `stream` like any other and can be captured in a CUDA graph;
+ * make the first call on a device outside stream capture).  Otherwise (other widths, or the float32 twin) float32 arithmetic
  * on the CUDA cores, one launch, no workspace.  Supported: dk, dv multiples of
  * 4, at most 512; other widths return RET_ERR_UNSUPPORTED.
  * retention_backward_f32 is the same with float32 q/k/v/dout/dq/dk/dv.

@@ -21,73 +21,31 @@
 // does a head with g <= 2^-64, where 1/(s g) could overflow and every other
 // power of g is negligible).
 //
-// So one call is: a gather kernel that stacks the permuted (and, for the
-// reversed problems, row-reversed) operands into batch-stacked tensors; a
-// kernel that prepares the starting states; one chunkwise forward per
-// operand shape (one when dk == dv, the three problems stacked on the batch
-// axis; two otherwise); and the same gather kernel run backwards to place the
-// results, then dS0 and the decay-0 term.  Scratch is allocated
-// stream-ordered on the caller's stream.
+// So one call is: a kernel that prepares the starting states, the three
+// forwards read straight from the caller's tensors and written straight into
+// the gradients (the chunkwise kernel's time-reversed mode takes the rows of
+// the second and third from the last to the first), then dS0 and the decay-0
+// term.  The three forwards are independent; they run on three streams (the
+// caller's and two of the library's own, forked and joined with events), each
+// planned for a third of the SMs, so together they fill the GPU like one
+// launch.  Scratch is allocated stream-ordered on the caller's stream.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
 namespace ret {
 namespace {
 
-constexpr int kMaxJobs = 9;
 // Decays at or below this are treated as 0 by the starting states: 1/(s g)
 // could overflow, and every power g^t with t >= 1 is below 2^-64 there, so
 // only the t = 0 term (added by zero_decay_term_kernel) is kept.
 constexpr float kTinyDecay = 5.42101086e-20f;  // 2^-64
-
-// Copy of a [BH][N][w] bf16 tensor into another, rows optionally reversed in
-// each head (row n of dst is row N-1-n of src).
-struct SeqJob {
-  const uint4* src;
-  uint4* dst;
-  int w16;      // row width in 16-byte units
-  int reverse;
-};
-struct SeqJobs {
-  SeqJob job[kMaxJobs];
-  int BH, N;
-};
-
-// grid: (row blocks of one head, head, job).  A block copies kRowIters
-// groups of `rows` = 256 / w16 rows; thread t moves 16-byte unit t % w16 of
-// row t / w16 of each group, so every row is one contiguous run of a warp's
-// stores and every load is a whole row of the source.
-constexpr int kRowIters = 4;
-__global__ void __launch_bounds__(256) seq_gather_kernel(const __grid_constant__ SeqJobs J) {
-  const SeqJob j = J.job[blockIdx.z];
-  const int w16 = j.w16;
-  const int rows = 256 / w16;  // rows per group
-  const int t = threadIdx.x;
-  const int r = t / w16, c = t - r * w16;
-  if (r >= rows) return;
-  const size_t head = (size_t)blockIdx.y * J.N;
-  const int n0 = blockIdx.x * rows * kRowIters + r;
-  uint4 x[kRowIters];
-#pragma unroll
-  for (int it = 0; it < kRowIters; ++it) {
-    const int n = n0 + it * rows;
-    if (n < J.N) {
-      const int sn = j.reverse ? J.N - 1 - n : n;
-      x[it] = __ldcs(j.src + (head + sn) * w16 + c);
-    }
-  }
-#pragma unroll
-  for (int it = 0; it < kRowIters; ++it) {
-    const int n = n0 + it * rows;
-    if (n < J.N) __stcs(j.dst + (head + n) * w16 + c, x[it]);
-  }
-}
 
 // Starting states and dS0: dst = f(h) * src or f(h) * src^T per head, src
 // [BH][r][c] float32 (NULL: zero), dst [BH][c][r] when transposed; f is 1,
@@ -172,25 +130,49 @@ int num_sms_current() {
   return n;
 }
 
-cudaError_t launch_seq(const SeqJobs& J, int n_jobs, cudaStream_t s) {
-  if (n_jobs == 0) return cudaSuccess;
-  int min_rows = 256;
-  for (int i = 0; i < n_jobs; ++i) min_rows = std::min(min_rows, 256 / J.job[i].w16);
-  const int blocks = (J.N + min_rows * kRowIters - 1) / (min_rows * kRowIters);
-  seq_gather_kernel<<<dim3(blocks, J.BH, n_jobs), 256, 0, s>>>(J);
-  return cudaGetLastError();
+// Two streams of the library's own per device, created on the first call
+// (make that call outside stream capture), and the events that fork the
+// gradient call's work onto them and join it back.  The lock is held while a
+// call enqueues, so the events are never re-recorded before the waits on
+// them are enqueued.
+constexpr int kMaxDevices = 64;
+struct Aux {
+  cudaStream_t st[2];
+  cudaEvent_t fork, join[2];
+  bool ready;
+};
+std::mutex g_aux_lock[kMaxDevices];
+Aux g_aux[kMaxDevices];
+
+cudaError_t aux_for(int dev, Aux** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  Aux& a = g_aux[dev];
+  if (!a.ready) {
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&a.st[i], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&a.join[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    a.ready = true;
+  }
+  *out = &a;
+  return cudaSuccess;
 }
 
-// One chunkwise forward over the batch-stacked problems of one operand shape.
-struct Group {
-  int parts;       // problems stacked on the batch axis
-  int dkp, dvp;    // the forward's query/key and value widths
+// The three forwards: 0 = dq (dout, v, k | S0^T), 1 = dk (v, dout, q |
+// dS^T/(s g), time reversed), 2 = dv (k, q, dout | dS/(s g), time reversed).
+struct Problem {
+  const void *q, *k, *v;
+  void* o;
+  int dkp, dvp;     // the forward's query/key and value widths
+  bool rev;
   ChunkPlan plan;
-  __nv_bfloat16 *q, *k, *v, *o;  // [parts*B][H][N][dkp or dvp]
-  float* state_in;               // [parts*B][H][dkp][dvp] or NULL
-  float* state_out;              // likewise, or NULL
-  float* ws;                     // segment scratch of the forward
+  float* state_in;  // or NULL (zero)
+  float* state_out; // or NULL
+  float* ws;
 };
+
+int backward_chunk(int N) { return N >= 4096 ? 128 : 64; }
 
 }  // namespace
 
@@ -204,122 +186,84 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
   const int sms = num_sms_current();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int BH = B * H;
-  if (BH > 65535) return cudaErrorNotSupported;  // heads on the gather grid's y axis
+  if (BH > 65535) return cudaErrorNotSupported;  // heads on the state kernels' grid y axis
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   const float scale = (float)(1.0 / std::sqrt((double)dk));
-  const int chunk = N >= 4096 ? 128 : 64;
-  const bool same = dk == dv;
-  // Problems: 0 = dq (dout, v, k | S0^T), 1 = dk (rev v, rev dout, rev q | dS^T/(s g)),
-  // 2 = dv (rev k, rev q, rev dout | dS/(s g)).  Problems 0 and 1 have the
-  // shape (dv, dk), problem 2 (dk, dv).
-  Group grp[2];
-  const int n_groups = same ? 1 : 2;
-  grp[0].parts = same ? 3 : 2;
-  grp[0].dkp = dv;
-  grp[0].dvp = dk;
-  if (!same) {
-    grp[1].parts = 1;
-    grp[1].dkp = dk;
-    grp[1].dvp = dv;
+  const int chunk = backward_chunk(N);
+  const int share = std::max(1, sms / 3);
+  Problem P[3] = {{dout, v, k, dq, dv, dk, false, {}, nullptr, nullptr, nullptr},
+                  {v, dout, q, dk_out, dv, dk, true, {}, nullptr, nullptr, nullptr},
+                  {k, q, dout, dv_out, dk, dv, true, {}, nullptr, nullptr, nullptr}};
+  const bool want_state[3] = {state_in != nullptr, dstate != nullptr, dstate != nullptr};
+  const size_t st_bytes = sizeof(float) * (size_t)BH * dk * dv;
+  size_t bytes = 0, off_in[3], off_ws[3], off_out = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (!chunk_tc_plan(B, H, N, P[i].dkp, P[i].dvp, chunk, share, &P[i].plan)) return cudaErrorNotSupported;
+    off_in[i] = bytes;
+    bytes += want_state[i] ? align256(st_bytes) : 0;
+    off_ws[i] = bytes;
+    bytes += align256(P[i].plan.workspace_bytes);
   }
-  const bool any_state = state_in != nullptr || dstate != nullptr;
-  size_t bytes = 0;
-  size_t off[2][7];
-  for (int gi = 0; gi < n_groups; ++gi) {
-    Group& G = grp[gi];
-    if (!chunk_tc_plan(G.parts * B, H, N, G.dkp, G.dvp, chunk, sms, &G.plan)) return cudaErrorNotSupported;
-    const size_t rows = (size_t)G.parts * BH * N, st = sizeof(float) * (size_t)G.parts * BH * G.dkp * G.dvp;
-    const size_t sz[7] = {rows * G.dkp * 2, rows * G.dkp * 2, rows * G.dvp * 2, rows * G.dvp * 2,
-                          any_state ? st : 0, dstate_in ? st : 0, G.plan.workspace_bytes};
-    for (int i = 0; i < 7; ++i) {
-      off[gi][i] = bytes;
-      bytes += align256(sz[i]);
-    }
+  if (dstate_in) {
+    off_out = bytes;
+    bytes += align256(st_bytes);
   }
   char* base = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, s);
-  if (e != cudaSuccess) return e;
-  for (int gi = 0; gi < n_groups; ++gi) {
-    Group& G = grp[gi];
-    G.q = reinterpret_cast<__nv_bfloat16*>(base + off[gi][0]);
-    G.k = reinterpret_cast<__nv_bfloat16*>(base + off[gi][1]);
-    G.v = reinterpret_cast<__nv_bfloat16*>(base + off[gi][2]);
-    G.o = reinterpret_cast<__nv_bfloat16*>(base + off[gi][3]);
-    G.state_in = any_state ? reinterpret_cast<float*>(base + off[gi][4]) : nullptr;
-    G.state_out = dstate_in ? reinterpret_cast<float*>(base + off[gi][5]) : nullptr;
-    G.ws = G.plan.workspace_bytes ? reinterpret_cast<float*>(base + off[gi][6]) : nullptr;
+  if (bytes > 0) {
+    e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, s);
+    if (e != cudaSuccess) return e;
   }
-  // where problem p lives: its group and its part inside the group
-  const int pg[3] = {0, 0, same ? 0 : 1}, pp[3] = {0, 1, same ? 2 : 0};
-  auto part_ptr = [&](__nv_bfloat16* t, int p, int width) {
-    return reinterpret_cast<uint4*>(t + (size_t)pp[p] * BH * N * width);
-  };
-  const uint4 *Q = static_cast<const uint4*>(q), *K = static_cast<const uint4*>(k), *V = static_cast<const uint4*>(v),
-              *DO = static_cast<const uint4*>(dout);
-  const int qk16 = dk / 8, v16 = dv / 8;
+  for (int i = 0; i < 3; ++i) {
+    P[i].state_in = want_state[i] ? reinterpret_cast<float*>(base + off_in[i]) : nullptr;
+    P[i].ws = P[i].plan.workspace_bytes ? reinterpret_cast<float*>(base + off_ws[i]) : nullptr;
+  }
+  if (dstate_in) P[2].state_out = reinterpret_cast<float*>(base + off_out);
 
-  // 1. operands: (query, key, value) of each problem
-  SeqJobs in{};
-  in.BH = BH;
-  in.N = N;
-  int nj = 0;
-  auto add = [&](SeqJobs& J, const uint4* src, uint4* dst, int w16, int rev) { J.job[nj++] = SeqJob{src, dst, w16, rev}; };
+  // 1. starting states: S0^T, dS^T/(s g), dS/(s g)
+  const int tiles = ((dk + 31) / 32) * ((dv + 31) / 32);
   {
-    Group &G0 = grp[pg[0]], &G1 = grp[pg[1]], &G2 = grp[pg[2]];
-    add(in, DO, part_ptr(G0.q, 0, G0.dkp), v16, 0);
-    add(in, V, part_ptr(G0.k, 0, G0.dkp), v16, 0);
-    add(in, K, part_ptr(G0.v, 0, G0.dvp), qk16, 0);
-    add(in, V, part_ptr(G1.q, 1, G1.dkp), v16, 1);
-    add(in, DO, part_ptr(G1.k, 1, G1.dkp), v16, 1);
-    add(in, Q, part_ptr(G1.v, 1, G1.dvp), qk16, 1);
-    add(in, K, part_ptr(G2.q, 2, G2.dkp), qk16, 1);
-    add(in, Q, part_ptr(G2.k, 2, G2.dkp), qk16, 1);
-    add(in, DO, part_ptr(G2.v, 2, G2.dvp), v16, 1);
-  }
-  e = launch_seq(in, nj, s);
-
-  // 2. starting states
-  if (e == cudaSuccess && any_state) {
-    for (int gi = 0; gi < n_groups && e == cudaSuccess; ++gi) {
-      Group& G = grp[gi];
-      StateJobs J{};
-      J.gamma = gamma;
-      J.H = H;
-      J.r = dk;
-      J.c = dv;
-      J.s = scale;
-      int n = 0;
-      for (int p = 0; p < 3; ++p) {
-        if (pg[p] != gi) continue;
-        float* dst = G.state_in + (size_t)pp[p] * BH * dk * dv;
-        if (p == 0) J.job[n++] = StateJob{state_in, dst, 1, kOne};
-        if (p == 1) J.job[n++] = StateJob{dstate, dst, 1, kInvSG};
-        if (p == 2) J.job[n++] = StateJob{dstate, dst, 0, kInvSG};
-      }
-      const int tiles = ((dk + 31) / 32) * ((dv + 31) / 32);
+    StateJobs J{};
+    J.gamma = gamma;
+    J.H = H;
+    J.r = dk;
+    J.c = dv;
+    J.s = scale;
+    int n = 0;
+    if (want_state[0]) J.job[n++] = StateJob{state_in, P[0].state_in, 1, kOne};
+    if (want_state[1]) J.job[n++] = StateJob{dstate, P[1].state_in, 1, kInvSG};
+    if (want_state[2]) J.job[n++] = StateJob{dstate, P[2].state_in, 0, kInvSG};
+    if (n > 0) {
       state_prep_kernel<<<dim3(tiles, BH, n), dim3(32, 8), 0, s>>>(J);
       e = cudaGetLastError();
     }
   }
 
-  // 3. the forwards
-  for (int gi = 0; gi < n_groups && e == cudaSuccess; ++gi) {
-    Group& G = grp[gi];
-    e = launch_chunk_tc(G.q, G.k, G.v, gamma, G.state_in, G.o, G.state_out, G.parts * B, H, N, G.dkp, G.dvp, G.plan,
-                        G.ws, nullptr, scale, s);
-  }
-
-  // 4. results into place: dq as is, dk and dv with their rows reversed back
+  // 2. the three forwards, forked onto three streams and joined back
   if (e == cudaSuccess) {
-    SeqJobs out{};
-    out.BH = BH;
-    out.N = N;
-    nj = 0;
-    add(out, part_ptr(grp[pg[0]].o, 0, grp[pg[0]].dvp), static_cast<uint4*>(dq), qk16, 0);
-    add(out, part_ptr(grp[pg[1]].o, 1, grp[pg[1]].dvp), static_cast<uint4*>(dk_out), qk16, 1);
-    add(out, part_ptr(grp[pg[2]].o, 2, grp[pg[2]].dvp), static_cast<uint4*>(dv_out), v16, 1);
-    e = launch_seq(out, nj, s);
+    std::lock_guard<std::mutex> hold(g_aux_lock[dev]);
+    Aux* a = nullptr;
+    e = aux_for(dev, &a);
+    if (e == cudaSuccess) e = cudaEventRecord(a->fork, s);
+    bool forked[2] = {false, false};
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaStreamWaitEvent(a->st[i], a->fork, 0);
+      forked[i] = e == cudaSuccess;
+    }
+    const cudaStream_t where[3] = {s, forked[0] ? a->st[0] : s, forked[1] ? a->st[1] : s};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+      e = launch_chunk_tc(P[i].q, P[i].k, P[i].v, gamma, P[i].state_in, P[i].o, P[i].state_out, B, H, N, P[i].dkp,
+                          P[i].dvp, P[i].plan, P[i].ws, nullptr, scale, where[i], nullptr, P[i].rev);
+    // join whatever was forked, whether or not every launch went in
+    for (int i = 0; i < 2; ++i) {
+      if (!forked[i]) continue;
+      cudaError_t ej = cudaEventRecord(a->join[i], a->st[i]);
+      if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, a->join[i], 0);
+      if (e == cudaSuccess) e = ej;
+    }
   }
-  // 5. dS0 = s g times the final state of the dv problem
+  // 3. dS0 = s g times the final state of the dv problem
   if (e == cudaSuccess && dstate_in) {
     StateJobs J{};
     J.gamma = gamma;
@@ -327,12 +271,11 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
     J.r = dk;
     J.c = dv;
     J.s = scale;
-    J.job[0] = StateJob{grp[pg[2]].state_out + (size_t)pp[2] * BH * dk * dv, dstate_in, 0, kSG};
-    const int tiles = ((dk + 31) / 32) * ((dv + 31) / 32);
+    J.job[0] = StateJob{P[2].state_out, dstate_in, 0, kSG};
     state_prep_kernel<<<dim3(tiles, BH, 1), dim3(32, 8), 0, s>>>(J);
     e = cudaGetLastError();
   }
-  // 6. decay-0 heads: the final-state gradient's last-token term
+  // 4. decay-0 heads: the final-state gradient's last-token term
   if (e == cudaSuccess && dstate) {
     zero_decay_term_kernel<<<BH, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(k),
                                               static_cast<const __nv_bfloat16*>(v), dstate, gamma,
@@ -340,22 +283,24 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
                                               static_cast<__nv_bfloat16*>(dv_out), H, N, dk, dv);
     e = cudaGetLastError();
   }
-  const cudaError_t e2 = cudaFreeAsync(base, s);
-  return e != cudaSuccess ? e : e2;
+  if (base) {
+    const cudaError_t e2 = cudaFreeAsync(base, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
 }
 
 int backward_tc_launches(int B, int H, int N, int dk, int dv, bool has_state_in, bool has_dstate, bool want_dstate_in) {
-  const int sms = 148;
-  const int chunk = N >= 4096 ? 128 : 64;
-  int n = 2;  // gather in, gather out
-  if (has_state_in || has_dstate) n += dk == dv ? 1 : 2;
+  const int share = 148 / 3;
+  const int chunk = backward_chunk(N);
+  int n = 0;
+  if (has_state_in || has_dstate) n += 1;  // starting states
   if (want_dstate_in) n += 1;
   if (has_dstate) n += 1;
-  const int groups = dk == dv ? 1 : 2;
-  for (int gi = 0; gi < groups; ++gi) {
+  const int w[3][2] = {{dv, dk}, {dv, dk}, {dk, dv}};
+  for (int i = 0; i < 3; ++i) {
     ChunkPlan plan;
-    const int parts = dk == dv ? 3 : (gi == 0 ? 2 : 1);
-    if (!chunk_tc_plan(parts * B, H, N, gi == 0 ? dv : dk, gi == 0 ? dk : dv, chunk, sms, &plan)) return -1;
+    if (!chunk_tc_plan(B, H, N, w[i][0], w[i][1], chunk, share, &plan)) return -1;
     n += chunk_tc_launch_count(plan);
   }
   return n;

@@ -476,7 +476,7 @@ __device__ __forceinline__ void load_qk(uint32_t sbase, const CUtensorMap* tmq, 
 // The four roles of a CTA (producer, MMA issuer, state group, output group).
 // FAST selects the rescaled form; a CTA picks one instantiation at its start,
 // so the code it runs holds no branches of the other form.
-template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM, bool ROT>
+template <int C, int DK, int DVT, bool SO, bool FAST, bool NORM, bool ROT, bool REV>
 __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x) {
   using L = Cfg<C, DK, DVT, SO>;
   constexpr int H = L::H, NQK = L::NQK, NV = L::NV, NP = L::NP, NO = L::NO, NSB = L::NSB;
@@ -499,13 +499,22 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   const int c_begin = seg * pos.seg_chunks;
   const int nck = min(c_begin + pos.seg_chunks, p.n_chunks) - c_begin;
   const int dv0 = dvt * DVT;
+  // Time reversed (rev): chunks are taken from the last to the first, and in
+  // a chunk of len tokens row r plays the part of row len-1-r of the causal
+  // form: in-chunk weights gamma^(c-r) for keys c >= r, gamma^(len-r) on the
+  // incoming state, gamma^r on the state update.
+  constexpr bool rev = REV;
+  static_assert(!(REV && (NORM || ROT)), "time reversal without GroupNorm or the rotation");
   const float g = p.gamma[head];
   const float lg = g > 0.f ? log2f(g) : 0.f;
   const bool zero_init = SO || (seg == 0 && p.state_in == nullptr);
   // The state-only pass walks its segment from the last chunk back to the
   // first (its sum does not depend on the order; the weights then need no
   // running rescale).  chunk_at(i) is the sequence chunk of the CTA's i-th step.
-  auto chunk_at = [&](int i) { return SO ? c_begin + nck - 1 - i : c_begin + i; };
+  auto chunk_at = [&](int i) {
+    const int j = SO ? c_begin + nck - 1 - i : c_begin + i;
+    return rev ? p.n_chunks - 1 - j : j;
+  };
   auto chunk_len = [&](int i) { return min(C, p.N - chunk_at(i) * C); };
   // Segment states in the workspace are stored lane-major: float4 number
   // (c4 * 128 + row) of block (cut unit, segment, half) holds columns
@@ -528,6 +537,9 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
   auto init_state = [&](int srow, uint32_t lane_addr, int cb0, int cb1) {
     if (seg > 0) griddep_wait();  // the pre-pass wrote the workspace
     const float seg_len = (float)pos.seg_chunks * (float)C;
+    // time reversed: the first segment holds the short chunk, so the caller's
+    // state (after the last token) is pad tokens closer to later segments
+    const float pad = rev && seg > 0 ? (float)(p.n_chunks * C - p.N) : 0.f;
 #pragma unroll 1
     for (int hh = 0; hh < H; ++hh) {
 #pragma unroll 1
@@ -539,7 +551,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         if (p.state_in != nullptr && row < p.dk) {
           // gamma^(seg Lseg) state_in, row hh*128 + srow, columns dv0 + 32 cb ..
           // (rows past dk and columns past dv are padding: they stay zero)
-          const float f = gamma_pow(g, lg, (float)seg * seg_len);
+          const float f = gamma_pow(g, lg, (float)seg * seg_len - pad);
           const int col = dv0 + cb * 32;
           const float4* src = reinterpret_cast<const float4*>(p.state_in + ((size_t)bh * p.dk + row) * p.dv + col);
 #pragma unroll
@@ -807,7 +819,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       if (!gw(L::bVFull + vs, (i / NV) & 1)) return false;
       const int len = chunk_len(i);
       scale_rows_bf16<L::kV, C>(sm + L::oV + vs * L::kV, et,
-                                [&](int r) { return r < len ? ci * pw[len - 1 - r] : 0.f; });
+                                [&](int r) { return r < len ? ci * pw[rev ? r : len - 1 - r] : 0.f; });
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bWReady + vs));
       return true;
@@ -819,10 +831,10 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       for (int hh = 0; hh < H; ++hh) {
         const int s = (i * H + hh) % NQK;
         scale_rows_bf16<L::kK, C>(sm + s * L::kQK + L::kQ, et,
-                                  [&](int r) { return r < len ? pw[len - 1 - r] : 0.f; });
+                                  [&](int r) { return r < len ? pw[rev ? r : len - 1 - r] : 0.f; });
         if (!SO)
-          scale_rows_bf16<(SO ? L::kK : L::kQ), C>(sm + s * L::kQK, et,
-                                                  [&](int r) { return r < len ? p.scale * pw[r + 1] : 0.f; });
+          scale_rows_bf16<(SO ? L::kK : L::kQ), C>(
+              sm + s * L::kQK, et, [&](int r) { return r < len ? p.scale * pw[rev ? len - r : r + 1] : 0.f; });
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bWReady + i % NV));
@@ -1056,12 +1068,15 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         for (int jj = 0; jj < 32; ++jj) {
           const int c0 = cb * 32 + 2 * jj;
           float a = __uint_as_float(r[2 * jj]), b = __uint_as_float(r[2 * jj + 1]);
+          // causal: key c <= query row; time reversed: key c >= query row
+          const int da = rev ? c0 - arow : arow - c0, db = rev ? c0 + 1 - arow : arow - c0 - 1;
+          const bool ka = arow >= 0 && da >= 0, kb = arow >= 0 && db >= 0;
           if (fast) {
-            a = c0 <= arow ? a : 0.f;
-            b = c0 + 1 <= arow ? b : 0.f;
+            a = ka ? a : 0.f;
+            b = kb ? b : 0.f;
           } else {
-            a = c0 <= arow ? pw[arow - c0] * p.scale * a : 0.f;
-            b = c0 + 1 <= arow ? pw[arow - c0 - 1] * p.scale * b : 0.f;
+            a = ka ? pw[da] * p.scale * a : 0.f;
+            b = kb ? pw[db] * p.scale * b : 0.f;
           }
           pk[jj] = pack_bf16(a, b);
         }
@@ -1081,7 +1096,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       tc_fence_after();
       const int len = chunk_len(i);
       float rt = 0.f;
-      if (arow >= 0 && arow < len) rt = fast ? p.scale / (ci * pw[len - 1 - arow]) : 1.f;
+      if (arow >= 0 && arow < len) rt = fast ? p.scale / (ci * pw[rev ? arow : len - 1 - arow]) : 1.f;
       const int vs = i % NV;
       uint8_t* stg = L::kSepStage ? sm + L::oStg : sm + L::oV + vs * L::kV;
       const uint32_t tO = tmem + lane_addr + L::cO + ob * DVT;
@@ -1155,7 +1170,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
       fence_proxy_async_smem();
       named_bar_sync(kBarO, kGroup);
       if (eo == 0) {
-        const int row0 = (c_begin + i) * C;
+        const int row0 = chunk_at(i) * C;
 #pragma unroll
         for (int b = 0; b < DVT / 64; ++b) {
           if constexpr (NORM)  // [B][N][H][dv]: (channel, head, token, batch row)
@@ -1241,7 +1256,8 @@ __device__ __forceinline__ void init_barriers(uint32_t sbase) {
   for (int i = 0; i < L::NQK; ++i) mbar_init(bar(L::bQkRot + i), kGroup);
 }
 
-template <int C, int DK, int DVT, bool SO, bool NORM, bool ROT>
+// REV: time reversed (out_m sums over keys n >= m; see chunk_roles).
+template <int C, int DK, int DVT, bool SO, bool NORM, bool ROT, bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -1279,7 +1295,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     prefetch_tensormap(&tmv);
     if (!SO) prefetch_tensormap(&tmo);
     for (int i = 0; i < pre; ++i) {
-      const int row = (SO ? c_begin + nck - 1 - i : c_begin + i) * C;  // the roles' chunk order
+      const int j = SO ? c_begin + nck - 1 - i : c_begin + i;  // the roles' chunk order
+      const int row = (REV ? p.n_chunks - 1 - j : j) * C;
       load_v<L, SO>(sbase, &tmv, i, row, pos.dvt * DVT, pos.bh);
       for (int hh = 0; hh < L::H; ++hh) load_qk<L, SO>(sbase, &tmq, &tmk, i * L::H + hh, hh, row, pos.bh);
     }
@@ -1302,8 +1319,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
   if (SO) griddep_launch_dependents();
 
   const RoleCtx x{&tmq, &tmk, &tmv, &tmo, sm, tmem, inv_gC, pre};
-  if (fast) chunk_roles<C, DK, DVT, SO, true, NORM, ROT>(p, x);
-  else chunk_roles<C, DK, DVT, SO, false, NORM, ROT>(p, x);
+  if (fast) chunk_roles<C, DK, DVT, SO, true, NORM, ROT, REV>(p, x);
+  else chunk_roles<C, DK, DVT, SO, false, NORM, ROT, REV>(p, x);
 
   // ---- teardown: every MMA has completed, every load landed, every store read ----
   tc_fence_before();
@@ -1374,11 +1391,11 @@ bool make_map_heads(CUtensorMap* m, const void* base, int dv, int H, int N, int 
   return r == CUDA_SUCCESS;
 }
 
-template <int C, int DK, int DVT, bool SO, bool NORM, bool ROT>
+template <int C, int DK, int DVT, bool SO, bool NORM, bool ROT, bool REV>
 cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mo, const TcParams& p, int grid, bool pdl, cudaStream_t s) {
   using L = Cfg<C, DK, DVT, SO>;
-  auto kern = chunk_tc_kernel<C, DK, DVT, SO, NORM, ROT>;
+  auto kern = chunk_tc_kernel<C, DK, DVT, SO, NORM, ROT, REV>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -1407,20 +1424,21 @@ cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return cudaGetLastError();
 }
 
-template <int C, int DK, int DVT, bool NORM, bool ROT>
+template <int C, int DK, int DVT, bool NORM, bool ROT, bool REV>
 cudaError_t launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   const bool split = p.segments > 1;
   const int n_cut = p.BH * p.n_dv_tiles - p.full_units;
   if (split) {
-    cudaError_t e = launch_one<C, DK, DVT, true, false, ROT>(mq, mk, mv, mo, p, n_cut * (p.segments - 1), false, s);
+    cudaError_t e = launch_one<C, DK, DVT, true, false, ROT, REV>(mq, mk, mv, mo, p, n_cut * (p.segments - 1), false, s);
     if (e != cudaSuccess) return e;
   }
-  return launch_one<C, DK, DVT, false, NORM, ROT>(mq, mk, mv, mo, p, p.full_units + n_cut * p.segments, split, s);
+  return launch_one<C, DK, DVT, false, NORM, ROT, REV>(mq, mk, mv, mo, p, p.full_units + n_cut * p.segments, split,
+                                                       s);
 }
 
 // The variant for these tile sizes.
-template <bool NORM>
+template <bool NORM, bool REV>
 cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s);
 
@@ -1430,27 +1448,27 @@ template <bool NORM, bool ROT>
 cudaError_t launch_variant(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
   if constexpr (ROT) {
-    if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
-                                               : launch_pair<64, 128, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
-    if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT>(mq, mk, mv, mo, p, s)
-                                               : launch_pair<64, 256, 64, NORM, ROT>(mq, mk, mv, mo, p, s);
+    if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, ROT, false>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<64, 128, 64, NORM, ROT, false>(mq, mk, mv, mo, p, s);
+    if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT, false>(mq, mk, mv, mo, p, s)
+                                               : launch_pair<64, 256, 64, NORM, ROT, false>(mq, mk, mv, mo, p, s);
     return cudaErrorNotSupported;
   } else {
-    return launch_variant_all<NORM>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
+    return launch_variant_all<NORM, false>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
   }
 }
 
-template <bool NORM>
+template <bool NORM, bool REV>
 cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
-  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, false>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<64, 128, 64, NORM, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, NORM, false>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<128, 128, 64, NORM, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, false>(mq, mk, mv, mo, p, s)
-                                             : launch_pair<64, 256, 64, NORM, false>(mq, mk, mv, mo, p, s);
-  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, false>(mq, mk, mv, mo, p, s)
-                                              : launch_pair<128, 256, 64, NORM, false>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dkt == 128) return t128 ? launch_pair<64, 128, 128, NORM, false, REV>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 128, 64, NORM, false, REV>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, NORM, false, REV>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 128, 64, NORM, false, REV>(mq, mk, mv, mo, p, s);
+  if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, false, REV>(mq, mk, mv, mo, p, s)
+                                             : launch_pair<64, 256, 64, NORM, false, REV>(mq, mk, mv, mo, p, s);
+  if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, false, REV>(mq, mk, mv, mo, p, s)
+                                              : launch_pair<128, 256, 64, NORM, false, REV>(mq, mk, mv, mo, p, s);
   return cudaErrorNotSupported;
 }
 
@@ -1515,9 +1533,11 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H, int N,
                             int dk, int dv, const ChunkPlan& plan, float* workspace,
-                            const ChunkNorm* norm, float scale, cudaStream_t s, const ChunkRotation* rot) {
+                            const ChunkNorm* norm, float scale, cudaStream_t s, const ChunkRotation* rot,
+                            bool rev) {
   const int BH = B * H;
   const int chunk = plan.chunk;
+  if (rev && (norm || rot)) return cudaErrorNotSupported;
   // GroupNorm statistics need a head's whole row, unpadded, in one CTA
   if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv)) return cudaErrorNotSupported;
   if (norm && rot) return cudaErrorNotSupported;
@@ -1550,6 +1570,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.n0 = rot ? rot->n0 : 0;
   const bool t128 = plan.dvt == 128;
   const int dkt = plan.dk_tile;
+  if (rev) return launch_variant_all<false, true>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
   if (norm) return launch_variant<true, false>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
   if (rot) return launch_variant<false, true>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
   return launch_variant<false, false>(chunk, dkt, t128, mq, mk, mv, mo, p, s);

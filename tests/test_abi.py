@@ -101,9 +101,9 @@ def test_chunkwise_shape_support(lib, dk, dv, chunk, want):
 
 
 def test_backward_launch_counts(lib):
-    """Kernels per bf16 gradient call: tensor-core widths gather, forward(s)
-    and place the results (plus the state kernels when states are given);
-    other widths take one CUDA-core launch."""
+    """Kernels per bf16 gradient call: tensor-core widths run three forwards
+    (plus the state kernels when states are given); other widths take one
+    CUDA-core launch."""
     n = ctypes.c_int(0)
     f = lib.retention_backward_launches
     assert f(4, 8, 2048, 128, 128, 0, 0, 0, ctypes.byref(n)) == binding.RET_OK and n.value == 3

@@ -60,9 +60,10 @@ def test_backward_matches_oracle(orc, B, H, N, dk, dv, states):
     _check(orc, q, k, v, g, dout, s0, ds, TOL_BF16, what=f"bf16 {B}x{H}x{N} {dk}/{dv}")
 
 
-def test_backward_any_decay_and_one_state(orc):
+@pytest.mark.parametrize("N", [170, 1000])  # 1000: the time-reversed forwards run in segments
+def test_backward_any_decay_and_one_state(orc, N):
     gam = [0.0, 0.5, 0.9, 1.0]
-    H, N, dk, dv = len(gam), 170, 64, 64
+    H, dk, dv = len(gam), 64, 64
     g = torch.tensor(gam, dtype=torch.float32)
     q, k, v, dout, s0, ds = _case(1, H, N, dk, dv, 6, torch.bfloat16, True)
     _check(orc, q, k, v, g, dout, s0, None, TOL_BF16, what="any decay, starting state only")
