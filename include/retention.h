@@ -277,6 +277,35 @@ int retention_chunkwise_noalloc(const void *q, const void *k, const void *v, con
                                 int B, int H, int N, int dk, int dv, int chunk, void *stream);
 
 /*
+ * retention_chunkwise_host -- retention_chunkwise with q, k, v, out and
+ * state_out in HOST memory (same shapes and layouts; gamma, H float32, is a
+ * device pointer).  The (batch row, head) pairs are cut into up to 8 slabs
+ * (whole batch rows; with B == 1, equal groups of heads); each slab is copied
+ * to the device, run by the chunkwise kernels and copied back on one of
+ * three streams the library creates per device on the first call (make it
+ * outside stream capture), so the copies in the two directions and the
+ * kernels of successive slabs overlap.  The streams are forked from and
+ * joined back to `stream` with events: the call is ordered on `stream` and
+ * only enqueues work, so the host buffers must stay valid, and out/state_out
+ * unread, until `stream` has reached that point.  Page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister) is needed for the copies to overlap;
+ * pageable memory gives the same results, serialised.  state_out may be NULL.
+ * dev_buffer: NULL (a device buffer is allocated stream-ordered on `stream`)
+ * or a 256-byte aligned device buffer of dev_buffer_bytes >= the size from
+ * retention_chunkwise_host_buffer_size.  Supported shapes: those of
+ * retention_chunkwise.  Each slab is planned on its own (its own split into
+ * segments), so results can differ from retention_chunkwise's in rounding
+ * order, within the same error bound.
+ */
+int retention_chunkwise_host(const void *q_host, const void *k_host, const void *v_host, const float *gamma,
+                             void *out_host, float *state_out_host,
+                             int B, int H, int N, int dk, int dv, int chunk,
+                             void *dev_buffer, size_t dev_buffer_bytes, void *stream);
+/* Device bytes retention_chunkwise_host needs for these sizes (three slab
+ * slots: q, k, v, out, state and segment scratch of one slab each).  Host only. */
+int retention_chunkwise_host_buffer_size(int B, int H, int N, int dk, int dv, int chunk, size_t *bytes);
+
+/*
  * retention_chunkwise_launches -- number of kernels one retention_chunkwise
  * call with these sizes enqueues (for launch accounting).  Host only.
  */

@@ -42,6 +42,8 @@ _SIGNATURES = {
                                ctypes.c_size_t, _vp],
     "retention_chunkwise_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_chunkwise_workspace_size": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)],
+    "retention_chunkwise_host": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t, _vp],
+    "retention_chunkwise_host_buffer_size": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)],
     "retention_chunkwise_launches": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)],
     "retention_chunkwise_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
     "retention_parallel": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp],
@@ -246,6 +248,51 @@ def retention_chunkwise_noalloc(q, k, v, gamma, chunk: int, out=None, state_out=
     args, out, state_out = _sequence_call("retention_chunkwise_noalloc", torch.bfloat16, q, k, v,
                                           gamma, out, state_out, want_state, [int(chunk)], stream)
     _check("retention_chunkwise_noalloc", lib().retention_chunkwise_noalloc(*args, _stream(stream)))
+    return out, state_out
+
+
+def _need_host(t, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+
+
+def chunkwise_host_buffer_size(B, H, N, dk, dv, chunk) -> int:
+    n = ctypes.c_size_t(0)
+    _check("retention_chunkwise_host_buffer_size",
+           lib().retention_chunkwise_host_buffer_size(B, H, N, dk, dv, chunk, ctypes.byref(n)))
+    return int(n.value)
+
+
+def retention_chunkwise_host(q, k, v, gamma, chunk: int, out=None, state_out=None, want_state: bool = True,
+                             buffer=None, stream=None):
+    """bf16 chunkwise forward of host (CPU, preferably pinned) q, k, v into host
+    out / state_out (allocated pinned when None); gamma is a CUDA tensor.  The
+    call only enqueues work: synchronise `stream` before reading the outputs.
+    `buffer`: optional uint8 CUDA tensor of chunkwise_host_buffer_size bytes."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q and v must be [B, H, N, d]")
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    _need_host(q, "q", torch.bfloat16, (B, H, N, dk))
+    _need_host(k, "k", torch.bfloat16, (B, H, N, dk))
+    _need_host(v, "v", torch.bfloat16, (B, H, N, dv))
+    _need(gamma, "gamma", torch.float32, (H,))
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.bfloat16).pin_memory()
+    _need_host(out, "out", torch.bfloat16, (B, H, N, dv))
+    if state_out is None and want_state:
+        state_out = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+    if state_out is not None:
+        _need_host(state_out, "state_out", torch.float32, (B, H, dk, dv))
+    buf_p = None if buffer is None else buffer.data_ptr()
+    buf_n = 0 if buffer is None else buffer.numel() * buffer.element_size()
+    _check("retention_chunkwise_host",
+           lib().retention_chunkwise_host(_p(q), _p(k), _p(v), _p(gamma), _p(out), _p(state_out), B, H, N, dk, dv,
+                                          int(chunk), buf_p, buf_n, _stream(stream)))
     return out, state_out
 
 

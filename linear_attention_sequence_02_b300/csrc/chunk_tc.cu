@@ -849,11 +849,14 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
         const uint32_t tS = tmem + lane_addr + L::cS + hh * DVT;
         const int u = i * H + hh, b = u % NSB;
         uint8_t* sb = sm + L::oSb + b * L::kSb;
-        if (u >= NSB && !gw(L::kMergeSbFree ? L::bOFull + b : L::bSbFree + b, (u / NSB - 1) & 1)) return false;
+        const bool sb_free = u < NSB;  // no earlier Q S product reads this buffer
+        auto wait_sb = [&] { return sb_free || gw(L::kMergeSbFree ? L::bOFull + b : L::bSbFree + b, (u / NSB - 1) & 1); };
+        const bool whole_row = has_state && fast && DVT == 128;
+        if (!whole_row && !wait_sb()) return false;
         if (has_state && i > 0 && !gw(L::bSFull + hh, (i - 1) & 1)) return false;
-        if (has_state && fast && DVT == 128) {
+        if (whole_row) {
           // the whole row in flight at once, so the state MMA is released
-          // before any of it is packed
+          // before any of it is packed, and before the snapshot buffer is free
           tc_fence_after();
           const float f = __uint_as_float((uint32_t)(127 - n) << 23);  // 2^-n
           uint32_t r[128];
@@ -862,6 +865,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar(L::bSRead + hh));  // the state MMA may overwrite S now
+          if (!wait_sb()) return false;
 #pragma unroll
           for (int cb = 0; cb < 4; cb += 2) {
             uint32_t pk[32];

@@ -207,3 +207,20 @@ def test_backward_validation(lib):
         # nothing to do: no tokens and no starting-state gradient wanted
         assert fn(None, None, None, None, None, None, None, None, None, None, None, 1, 1, 0, 64, 64, None) == \
             binding.RET_OK
+
+
+def test_host_entry_validation_and_buffer_size(lib):
+    """retention_chunkwise_host rejects missing or misaligned arguments before
+    it touches the device; its buffer size covers three slab slots."""
+    f = lib.retention_chunkwise_host
+    assert f(None, P, P, P, P, None, 1, 1, 8, 64, 64, 64, None, 0, None) == binding.RET_ERR_INVALID
+    assert f(P, P, P, P, P, None, 0, 1, 8, 64, 64, 64, None, 0, None) == binding.RET_ERR_INVALID
+    assert f(P, P, P, P, P, None, 1, 1, 8, 64, 64, 64, P_ODD, 1 << 20, None) == binding.RET_ERR_INVALID
+    n = ctypes.c_size_t(0)
+    g = lib.retention_chunkwise_host_buffer_size
+    assert g(8, 16, 8192, 256, 512, 128, ctypes.byref(n)) == binding.RET_OK
+    # one batch row a slab: q, k, v, out and the state of 16 heads, three times
+    per_slot = 16 * 8192 * (2 * 256 + 2 * 512) * 2 + 16 * 256 * 512 * 4
+    assert 3 * per_slot <= n.value < 3 * per_slot + (64 << 20)
+    assert g(1, 2, 100, 72, 64, 64, ctypes.byref(n)) == binding.RET_ERR_UNSUPPORTED
+    assert g(1, 2, 100, 64, 64, 64, None) == binding.RET_ERR_INVALID
