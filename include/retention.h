@@ -86,8 +86,10 @@ typedef enum {
  * multiple of 16 in [16, 1024]; N >= 0.  Other shapes return
  * RET_ERR_UNSUPPORTED.  The chunk length is a tiling choice that does not
  * change the result (every chunk length computes the same sums, up to
- * rounding order); chunk 32 runs on 64-token tiles, the tensor cores'
- * smallest tile height.  Widths below the kernel's tile (128 or 256 query
+ * rounding order), so the kernels pick their tile height, 64 or 128 tokens,
+ * from the sizes whatever chunk is asked for: 128 (the tensor cores' full
+ * tile height), unless 64-token tiles give more CTAs (a short sequence with
+ * few heads).  Widths below the kernel's tile (128 or 256 query
  * and key columns, 64 or 128 value columns) are padded with zeros by the
  * loads, which leaves every product unchanged.  The work is cut into units,
  * one per (batch row, head, value tile).  With fewer units than SMs every
@@ -128,13 +130,13 @@ int retention_chunkwise_from_state(const void *q, const void *k, const void *v, 
  * retention_chunkwise_rotated -- retention_chunkwise_from_state of the queries
  * and keys turned by the position phase rotation of "2. Relative Position via
  * Complex Exponential Phase Rotations" (as retention_rotate below, with the
- * same theta and n0 for q and k).  With 64-token tiles (chunk 32 or 64) and
- * one value tile per head (dv of at most 64, or exactly 128), the
- * rotation is fused into the kernels' load stage: each Q/K tile is turned in
- * shared memory after it lands and before the tensor cores read it, so q and
- * k are read from HBM once and the turned copies are never written.  For
- * other shapes (128-token tiles, several value tiles per head) that fusion
- * measured slower than separate passes, so q and k are turned into a
+ * same theta and n0 for q and k).  With one value tile per head (dv of at
+ * most 64, or exactly 128), the rotation is fused into the kernels' load
+ * stage: each Q/K tile is turned in shared memory after it lands and before
+ * the tensor cores read it, so q and k are read from HBM once and the turned
+ * copies are never written.  With several value tiles per head (each would
+ * turn the same Q/K tiles) that fusion measured slower than separate
+ * passes, so q and k are turned into a
  * stream-ordered scratch buffer (cudaMallocAsync / cudaFreeAsync on
  * `stream`) by the standalone rotation first.  Either way:
  *

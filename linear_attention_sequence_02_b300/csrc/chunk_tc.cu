@@ -1446,8 +1446,7 @@ template <bool NORM, bool REV>
 cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                                const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s);
 
-// The fused rotation is built for 64-token tiles only (the shapes where it
-// pays; see retention_chunkwise_rotated).
+// The variants for these tile sizes (with the fused rotation, or without it).
 template <bool NORM, bool ROT>
 cudaError_t launch_variant(int chunk, int dkt, bool t128, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mo, const TcParams& p, cudaStream_t s) {
@@ -1456,6 +1455,10 @@ cudaError_t launch_variant(int chunk, int dkt, bool t128, const CUtensorMap& mq,
                                                : launch_pair<64, 128, 64, NORM, ROT, false>(mq, mk, mv, mo, p, s);
     if (chunk == 64 && dkt == 256) return t128 ? launch_pair<64, 256, 128, NORM, ROT, false>(mq, mk, mv, mo, p, s)
                                                : launch_pair<64, 256, 64, NORM, ROT, false>(mq, mk, mv, mo, p, s);
+    if (chunk == 128 && dkt == 128) return t128 ? launch_pair<128, 128, 128, NORM, ROT, false>(mq, mk, mv, mo, p, s)
+                                                : launch_pair<128, 128, 64, NORM, ROT, false>(mq, mk, mv, mo, p, s);
+    if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, ROT, false>(mq, mk, mv, mo, p, s)
+                                                : launch_pair<128, 256, 64, NORM, ROT, false>(mq, mk, mv, mo, p, s);
     return cudaErrorNotSupported;
   } else {
     return launch_variant_all<NORM, false>(chunk, dkt, t128, mq, mk, mv, mo, p, s);
@@ -1485,21 +1488,61 @@ std::atomic<unsigned int> g_test_stall_us{0};
 
 int chunk_tc_launch_count(const ChunkPlan& plan) { return plan.launches; }
 
+namespace {
+
+// The split of a plan with tile height `tile`: segments, chunks per segment,
+// cut units and their workspace (see chunk_tc_plan).
+struct Split {
+  int n_chunks, segs, seg_chunks;
+  long long cut;
+  size_t ws;
+};
+Split split_for(long long units, int N, int tile, int num_sms, int dk_tile, int dvt, size_t ws_limit) {
+  Split r;
+  r.n_chunks = (N + tile - 1) / tile;
+  r.cut = units;
+  int segs = 1;
+  if (num_sms > 0 && units < num_sms) {
+    segs = (int)(num_sms / units);
+  } else if (num_sms > 0 && units % num_sms != 0) {
+    r.cut = units % num_sms;
+    segs = (int)(num_sms / r.cut);
+  }
+  segs = std::max(1, std::min(segs, r.n_chunks / 4));
+  int seg_chunks = r.n_chunks > 0 ? (r.n_chunks + segs - 1) / segs : 1;
+  if (r.n_chunks > 0) segs = (r.n_chunks + seg_chunks - 1) / seg_chunks;  // no empty segment
+  // segment states cover the padded tile (dk_tile rows, dvt columns) of each cut unit
+  r.ws = segs > 1 ? sizeof(float) * (size_t)r.cut * (segs - 1) * dk_tile * (size_t)dvt : 0;
+  if (segs <= 1 || (r.cut < units && r.ws > ws_limit)) {
+    segs = 1;
+    seg_chunks = std::max(1, r.n_chunks);
+    r.cut = units;
+    r.ws = 0;
+  }
+  r.segs = segs;
+  r.seg_chunks = std::max(1, seg_chunks);
+  return r;
+}
+
+}  // namespace
+
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan,
-                   size_t ws_limit) {
-  // chunk 32 runs on 64-token tiles: the chunk length is a tiling choice that
-  // leaves the result unchanged (every chunk length computes the same sums),
-  // and the tensor cores' smallest tile has 64 rows.
+                   size_t ws_limit, int tile) {
+  // The chunk length is a tiling choice that leaves the result unchanged
+  // (every chunk length computes the same sums, up to rounding order), so the
+  // kernels run 128-token tiles (full-height tensor-core tiles, half as many
+  // per-chunk steps as 64-token ones: mid -10%, its gradients -9%), unless
+  // 64-token tiles give more CTAs (a short sequence with few units, where the
+  // segments are capped at n_chunks / 4) or the caller fixes the tile.
   if (!(chunk == 32 || chunk == 64 || chunk == 128)) return false;
+  if (!(tile == 0 || tile == 64 || tile == 128)) return false;
   if (dk < 16 || dk > 256 || dk % 16 != 0) return false;
   if (dv < 16 || dv > 1024 || dv % 16 != 0) return false;
   if (N < 0) return false;
   const int dvt = pick_dvt(dv);
-  plan->chunk = chunk == 32 ? 64 : chunk;
   plan->dk_tile = dk <= 128 ? 128 : 256;
   plan->dvt = dvt;
   plan->n_dv_tiles = (dv + dvt - 1) / dvt;
-  plan->n_chunks = (N + plan->chunk - 1) / plan->chunk;
   const long long units = (long long)B * H * plan->n_dv_tiles;
   if (units > (1LL << 30)) return false;
   // Enough segments that every SM gets a CTA, each segment at least 4 chunks:
@@ -1507,30 +1550,23 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   // last, partial wave are cut so that it holds about as many CTAs as there
   // are SMs (the other units run whole), if their segment states fit within
   // ws_limit bytes.
-  long long cut = units;
-  int segs = 1;
-  if (num_sms > 0 && units < num_sms) {
-    segs = (int)(num_sms / units);
-  } else if (num_sms > 0 && units % num_sms != 0) {
-    cut = units % num_sms;
-    segs = (int)(num_sms / cut);
+  Split sp = split_for(units, N, tile ? tile : 128, num_sms, plan->dk_tile, dvt, ws_limit);
+  plan->chunk = tile ? tile : 128;
+  if (tile == 0) {
+    const Split s64 = split_for(units, N, 64, num_sms, plan->dk_tile, dvt, ws_limit);
+    auto ctas = [&](const Split& x) { return units - x.cut + x.cut * x.segs; };
+    if (ctas(s64) > ctas(sp)) {
+      sp = s64;
+      plan->chunk = 64;
+    }
   }
-  segs = std::max(1, std::min(segs, plan->n_chunks / 4));
-  int seg_chunks = plan->n_chunks > 0 ? (plan->n_chunks + segs - 1) / segs : 1;
-  if (plan->n_chunks > 0) segs = (plan->n_chunks + seg_chunks - 1) / seg_chunks;  // no empty segment
-  // segment states cover the padded tile (dk_tile rows, dvt columns) of each cut unit
-  const size_t ws = segs > 1 ? sizeof(float) * (size_t)cut * (segs - 1) * plan->dk_tile * (size_t)dvt : 0;
-  if (segs <= 1 || (cut < units && ws > ws_limit)) {
-    segs = 1;
-    seg_chunks = std::max(1, plan->n_chunks);
-    cut = units;
-  }
-  plan->segments = segs;
-  plan->seg_chunks = std::max(1, seg_chunks);
-  plan->full_units = segs > 1 ? (int)(units - cut) : (int)units;
-  plan->workspace_bytes = segs > 1 ? ws : 0;
-  plan->launches = segs > 1 ? 2 : 1;
-  if (plan->full_units + cut * segs > INT32_MAX) return false;
+  plan->n_chunks = sp.n_chunks;
+  plan->segments = sp.segs;
+  plan->seg_chunks = sp.seg_chunks;
+  plan->full_units = sp.segs > 1 ? (int)(units - sp.cut) : (int)units;
+  plan->workspace_bytes = sp.ws;
+  plan->launches = sp.segs > 1 ? 2 : 1;
+  if (plan->full_units + sp.cut * sp.segs > INT32_MAX) return false;
   return true;
 }
 

@@ -38,7 +38,7 @@ cudaError_t launch_chunkwise_f32(const float* q, const float* k, const float* v,
 // columns x `rows` rows and 128-byte swizzle; boxes past the ends read zeros.
 bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows);
 struct ChunkPlan {
-  int chunk;        // tokens per tile (64 or 128; a requested chunk of 32 runs as 64)
+  int chunk;        // tokens per tile (64 or 128, whatever chunk was asked for)
   int dk_tile;      // query/key columns the kernel is built for (128 or 256; dk <= dk_tile)
   int dvt;          // value columns per CTA (64 or 128)
   int n_dv_tiles;   // ceil(dv / dvt); the last tile's columns past dv are padding
@@ -53,8 +53,10 @@ struct ChunkPlan {
 // When there are more units than SMs, the units of the last, partial wave are
 // cut into segments only if their segment states take at most ws_limit bytes
 // (otherwise every unit runs whole and no workspace is needed).
+// tile: 0 lets the plan pick the tile height (64 or 128 tokens, see
+// chunk_tc.cu), 64 or 128 fixes it.
 bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, ChunkPlan* plan,
-                   size_t ws_limit = SIZE_MAX);
+                   size_t ws_limit = SIZE_MAX, int tile = 0);
 // Workspace bytes of the plan that retention_chunkwise_ws runs when given at
 // most `limit` bytes (a RET_* status; plans on the current device).
 int chunkwise_workspace_within(int B, int H, int N, int dk, int dv, int chunk, size_t limit, size_t* bytes);
