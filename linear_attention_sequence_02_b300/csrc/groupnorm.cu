@@ -278,7 +278,7 @@ cudaError_t launch_groupnorm_bf16(const void* r, const float* weight, const floa
   if (a16) {
     if (dv <= 32) return launch_vec<4, 1, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
     if (dv <= 64) return launch_vec<8, 1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
-    if (dv <= 128) return launch_vec<16, 1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
+    if (dv <= 128) return launch_vec<16, 1, 8>(r, weight, bias, y, B, H, N, dv, eps, sms, s);  // 12.3 us against 14.3 with 4
     if (dv <= 256) return launch_vec<32, 1, 4>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
     if (dv <= 512) return launch_vec<32, 2, 2>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
     return launch_vec<32, 4, 1>(r, weight, bias, y, B, H, N, dv, eps, sms, s);
