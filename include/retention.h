@@ -82,16 +82,17 @@ typedef enum {
  * zero.  If state_out is not NULL it receives the state after token N-1
  * (zero when N == 0).
  *
- * Supported: chunk in {32, 64, 128}; dk a multiple of 16 in [16, 256]; dv a
+ * Supported: chunk in {32, 64, 128}; dk a multiple of 16 in [16, 512]; dv a
  * multiple of 16 in [16, 1024]; N >= 0.  Other shapes return
  * RET_ERR_UNSUPPORTED.  The chunk length is a tiling choice that does not
  * change the result (every chunk length computes the same sums, up to
  * rounding order), so the kernels pick their tile height, 64 or 128 tokens,
  * from the sizes whatever chunk is asked for: 128 (the tensor cores' full
  * tile height), unless 64-token tiles give more CTAs (a short sequence with
- * few heads).  Widths below the kernel's tile (128 or 256 query
- * and key columns, 64 or 128 value columns) are padded with zeros by the
- * loads, which leaves every product unchanged.  The work is cut into units,
+ * few heads); above 256 query/key columns the tiles are 512 columns wide,
+ * 64 tokens high, with 64-wide value tiles.  Widths below the kernel's tile
+ * (128, 256 or 512 query and key columns, 64 or 128 value columns) are
+ * padded with zeros by the loads, which leaves every product unchanged.  The work is cut into units,
  * one per (batch row, head, value tile).  With fewer units than SMs every
  * unit's sequence is split into segments; with more, only the units of the
  * last, partial wave are split (so that wave holds about one CTA per SM).
@@ -392,7 +393,7 @@ int retention_step_rotated(const void *q, const void *k, const void *v, const fl
  * gradient, or dstate_in equal to dstate or state_in, returns
  * RET_ERR_INVALID.  When N == 0, dstate_in receives a copy of dstate (zero if
  * NULL).
- * How it runs: with bf16 tensors and dk, dv multiples of 16 in [16, 256], on
+ * How it runs: with bf16 tensors and dk, dv multiples of 16 in [16, 512], on
  * the tensor cores, each gradient as a chunkwise forward of permuted
  * operands (dq the forward of (dout, v, k) from S0^T; dk and dv the
  * time-reversed forwards of (v, dout, q) and (k, q, dout) from dstate^T/(s g)

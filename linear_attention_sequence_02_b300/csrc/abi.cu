@@ -90,8 +90,9 @@ int chunkwise_alloc(const void* q, const void* k, const void* v, const float* ga
   if (sms <= 0) return RET_ERR_CUDA;
   st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
   if (st != RET_OK) return st;
-  // GroupNorm: a head's whole row, unpadded, in one CTA (dv of 64 or 128)
-  if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv)) return RET_ERR_UNSUPPORTED;
+  // GroupNorm: a head's whole row, unpadded, in one CTA (dv of 64 or 128),
+  // with query/key tiles of at most 256 columns
+  if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv || plan.dk_tile > 256)) return RET_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) {
     // the state after no tokens is the state before them
@@ -293,7 +294,7 @@ int retention_chunkwise_rotated(const void* q, const void* k, const void* v, con
   if (sms <= 0) return RET_ERR_CUDA;
   st = plan_chunkwise(B, H, N, dk, dv, chunk, sms, &plan);
   if (st != RET_OK) return st;
-  if (N == 0 || plan.n_dv_tiles == 1)
+  if (N == 0 || (plan.n_dv_tiles == 1 && plan.dk_tile <= 256))
     return chunkwise_alloc(q, k, v, gamma, state_in, out, state_out, B, H, N, dk, dv, chunk, nullptr, stream, &rot);
   if (!ret::rotate_supported(N, dk, n0)) return RET_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

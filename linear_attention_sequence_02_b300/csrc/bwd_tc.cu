@@ -177,7 +177,7 @@ int backward_chunk(int N) { return N >= 4096 ? 128 : 64; }
 }  // namespace
 
 bool backward_tc_supported(int dk, int dv) {
-  return dk % 16 == 0 && dv % 16 == 0 && dk >= 16 && dv >= 16 && dk <= 256 && dv <= 256;
+  return dk % 16 == 0 && dv % 16 == 0 && dk >= 16 && dv >= 16 && dk <= 512 && dv <= 512;
 }
 
 cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, const float* gamma, const float* state_in,

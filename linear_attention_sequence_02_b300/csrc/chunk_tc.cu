@@ -106,7 +106,11 @@ __device__ __forceinline__ int acc_row(int M, int quarter, int lane) {
 template <int C, int DK, int DVT, bool SO>
 struct Cfg {
   static_assert(C == 64 || C == 128, "chunk");
-  static_assert(DK == 128 || DK == 256, "dk");
+  static_assert(DK == 128 || DK == 256 || DK == 512, "dk");
+  // 512-wide queries and keys: four 128-column halves of the state (256 TMEM
+  // columns at 64-wide value tiles) and 64-token tiles, so the Q/K ring holds
+  // more than one chunk
+  static_assert(DK < 512 || (C == 64 && DVT == 64), "512-wide keys: 64-token tiles, 64-wide value tiles");
   static_assert(DVT == 64 || DVT == 128, "value tile");
   static constexpr int kC = C, kDVT = DVT;
   static constexpr int H = DK / 128;                  // 128-row halves of the state
@@ -155,6 +159,7 @@ struct Cfg {
   static_assert(kQK % 1024 == 0 && kV % 1024 == 0 && kSb % 1024 == 0, "align");
   // state_out is staged through the (then idle) rings: rows of DVT + 4 floats
   static constexpr int kStageRow = DVT + 4;
+  static_assert(SO || H * 128 * kStageRow * 4 <= kAlloc, "state_out staging");
   // tensor memory: state halves, P buffers, output buffers
   static constexpr int kSCols = H * DVT;
   // Where only one of them fits twice, two O buffers (the outputs of chunk i
@@ -1476,6 +1481,9 @@ cudaError_t launch_variant_all(int chunk, int dkt, bool t128, const CUtensorMap&
                                              : launch_pair<64, 256, 64, NORM, false, REV>(mq, mk, mv, mo, p, s);
   if (chunk == 128 && dkt == 256) return t128 ? launch_pair<128, 256, 128, NORM, false, REV>(mq, mk, mv, mo, p, s)
                                               : launch_pair<128, 256, 64, NORM, false, REV>(mq, mk, mv, mo, p, s);
+  if constexpr (!NORM) {
+    if (chunk == 64 && dkt == 512 && !t128) return launch_pair<64, 512, 64, false, false, REV>(mq, mk, mv, mo, p, s);
+  }
   return cudaErrorNotSupported;
 }
 
@@ -1536,11 +1544,15 @@ bool chunk_tc_plan(int B, int H, int N, int dk, int dv, int chunk, int num_sms, 
   // segments are capped at n_chunks / 4) or the caller fixes the tile.
   if (!(chunk == 32 || chunk == 64 || chunk == 128)) return false;
   if (!(tile == 0 || tile == 64 || tile == 128)) return false;
-  if (dk < 16 || dk > 256 || dk % 16 != 0) return false;
+  if (dk < 16 || dk > 512 || dk % 16 != 0) return false;
   if (dv < 16 || dv > 1024 || dv % 16 != 0) return false;
   if (N < 0) return false;
-  const int dvt = pick_dvt(dv);
-  plan->dk_tile = dk <= 128 ? 128 : 256;
+  // above 256 query/key columns: 512-wide tiles with 64-token, 64-wide value tiles
+  const bool wide = dk > 256;
+  if (wide && tile == 128) return false;
+  if (wide) tile = 64;
+  const int dvt = wide ? 64 : pick_dvt(dv);
+  plan->dk_tile = dk <= 128 ? 128 : dk <= 256 ? 256 : 512;
   plan->dvt = dvt;
   plan->n_dv_tiles = (dv + dvt - 1) / dvt;
   const long long units = (long long)B * H * plan->n_dv_tiles;

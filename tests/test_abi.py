@@ -83,7 +83,7 @@ def test_chunkwise_rejects_bad_arguments_on_host(lib, args, want):
     (128, 128, 256, binding.RET_ERR_UNSUPPORTED),
     (72, 128, 64, binding.RET_ERR_UNSUPPORTED),     # d_k not a multiple of 16
     (8, 128, 64, binding.RET_ERR_UNSUPPORTED),
-    (272, 128, 64, binding.RET_ERR_UNSUPPORTED),    # d_k above 256
+    (528, 128, 64, binding.RET_ERR_UNSUPPORTED),    # d_k above 512
     (128, 24, 64, binding.RET_ERR_UNSUPPORTED),     # d_v not a multiple of 16
     (128, 1040, 64, binding.RET_ERR_UNSUPPORTED),   # d_v above 1024
 ])

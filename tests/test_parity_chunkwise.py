@@ -45,6 +45,10 @@ CASES = [
     (1, 2, 2100, 48, 208, 64),    # segments, d_v = 208 (four 64-wide tiles, the last one 16 wide)
     (1, 2, 301, 128, 128, 32),    # chunk 32 (runs on 64-token tiles)
     (1, 1, 2500, 80, 144, 32),    # chunk 32 with segments and padded widths
+    # query/key widths above 256: 512-wide tiles, 64-token and 64-wide value tiles
+    (1, 2, 300, 512, 128, 128),   # chunk 128 asked for, run on 64-token tiles
+    (2, 2, 333, 384, 64, 64),     # d_k = 384: the last 128 columns padding
+    (1, 1, 2100, 512, 80, 64),    # segments, padded value tile
 ]
 
 
