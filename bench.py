@@ -28,12 +28,12 @@ Also reported on the same line:
               d_v=256, fp32 state (128 MiB > L2): 1024 sequential steps
               captured in one CUDA graph; steps/s and HBM roofline.
   groupnorm, rotate, mid_groupnorm_fused, mid_rotated, mid_backward,
-  mid_parallel, long_parallel   the other kernels.
+  7b_backward, mid_parallel, long_parallel   the other kernels.
 
 `--impl reference` times the fp64 CPU oracle alone on the same workload and
 metric (one batch row of the 7B-shaped workload per step, scaled to the
 batch) and prints its own line.
-`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b,parallel,parallel_long,rotated}`
+`--only {mid,long,7b,decode,groupnorm,rotate,backward,backward_long,backward_7b,parallel,parallel_long,rotated,e2e}`
 runs one workload alone and prints its timing
 (used to give ncu a small, single-workload command).
 Under torchrun each rank runs its own replica (independent batches, no
@@ -770,6 +770,20 @@ def run_ours(args):
                          "algorithmic_bytes_per_call": bbytes,
                          "tensor_flops_frac": round(backward_flops(MID) / bt / 1e12 / tflops, 4)},
             "gpu_launches": binding.backward_launches(MID["B"], MID["H"], MID["N"], MID["dk"], MID["dv"])}
+        # gradients of the 7B-shaped workload (512-wide queries in the dq and dk forwards)
+        bt7 = statistics.median(time_backward(B7, 5, dev, flush)) / 1e3
+        b7bytes = backward_bytes(B7)
+        extra["7b_backward"] = {
+            "tokens_per_s": round(B7["B"] * B7["N"] / bt7, 1), "ms_per_call": round(bt7 * 1e3, 5),
+            "config": {"workload": "7B-shaped retention gradients (dq, dk, dv), no states", "B": B7["B"], "H": B7["H"],
+                       "N": B7["N"], "dk": B7["dk"], "dv": B7["dv"], "chunk": backward_chunk(B7),
+                       "l2": "flushed before each call (512 MiB write, then 512 MiB read)",
+                       "timing": "CUDA graph replay of the call"},
+            "roofline": {"bound": "tensor", "achieved": round(backward_flops(B7) / bt7 / 1e12, 1), "peak": tflops,
+                         "unit": "TFLOP/s", "frac": round(backward_flops(B7) / bt7 / 1e12 / tflops, 4),
+                         "traffic": None, "algorithmic_flops_per_call": backward_flops(B7),
+                         "hbm_frac": round(b7bytes / bt7 / 1e9 / hbm, 4)},
+            "gpu_launches": binding.backward_launches(B7["B"], B7["H"], B7["N"], B7["dk"], B7["dv"])}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
