@@ -29,6 +29,15 @@
 // caller's and two of the library's own, forked and joined with events), each
 // planned for a third of the SMs, so together they fill the GPU like one
 // launch.  Scratch is allocated stream-ordered on the caller's stream.
+//
+// A forward is linear in a split of its query/key width: with q = [q1 q2] and
+// k = [k1 k2], (q_n . k_m) = (q1_n . k1_m) + (q2_n . k2_m) and the state's
+// rows split the same way, so the forward of (q, k, v) from S is the sum of
+// the forwards of (q1, k1, v) from S's first rows and (q2, k2, v) from the
+// rest.  Forwards whose query/key width is above 256 (dq's and dk's when
+// dv > 256) run as 256-column parts on the 128-token tiles (read in place
+// with the row stride of the full width), the first part into the gradient,
+// the others into scratch, then summed into it.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -161,16 +170,38 @@ cudaError_t aux_for(int dev, Aux** out) {
 
 // The three forwards: 0 = dq (dout, v, k | S0^T), 1 = dk (v, dout, q |
 // dS^T/(s g), time reversed), 2 = dv (k, q, dout | dS/(s g), time reversed).
+constexpr int kPartWidth = 256;  // query/key columns of one part of a wide forward
+constexpr int kMaxParts = 2;     // widths up to 512
 struct Problem {
   const void *q, *k, *v;
   void* o;
   int dkp, dvp;     // the forward's query/key and value widths
   bool rev;
-  ChunkPlan plan;
+  int parts;        // ceil(dkp / kPartWidth)
+  ChunkPlan plan[kMaxParts];
   float* state_in;  // or NULL (zero)
   float* state_out; // or NULL
-  float* ws;
+  float* ws[kMaxParts];
+  __nv_bfloat16* partial[kMaxParts];  // outputs of parts 1.. (part 0 writes o)
 };
+
+// dst += src, bf16, n elements (a multiple of 8, both 16-byte aligned).
+__global__ void __launch_bounds__(256) add_bf16_kernel(__nv_bfloat16* dst, const __nv_bfloat16* src, size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    uint4 a = reinterpret_cast<uint4*>(dst)[i];
+    const uint4 b = reinterpret_cast<const uint4*>(src)[i];
+    uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
+    const uint32_t* pb = reinterpret_cast<const uint32_t*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[e]));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[e]));
+      const __nv_bfloat162 z = __floats2bfloat162_rn(x.x + y.x, x.y + y.y);
+      pa[e] = *reinterpret_cast<const uint32_t*>(&z);
+    }
+    reinterpret_cast<uint4*>(dst)[i] = a;
+  }
+}
 
 int backward_chunk(int N) { return N >= 4096 ? 128 : 64; }
 
@@ -193,18 +224,34 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
   const float scale = (float)(1.0 / std::sqrt((double)dk));
   const int chunk = backward_chunk(N);
   const int share = std::max(1, sms / 3);
-  Problem P[3] = {{dout, v, k, dq, dv, dk, false, {}, nullptr, nullptr, nullptr},
-                  {v, dout, q, dk_out, dv, dk, true, {}, nullptr, nullptr, nullptr},
-                  {k, q, dout, dv_out, dk, dv, true, {}, nullptr, nullptr, nullptr}};
+  Problem P[3] = {};
+  const void* ops[3][4] = {{dout, v, k, dq}, {v, dout, q, dk_out}, {k, q, dout, dv_out}};
+  const int widths[3][2] = {{dv, dk}, {dv, dk}, {dk, dv}};
+  for (int i = 0; i < 3; ++i) {
+    P[i].q = ops[i][0];
+    P[i].k = ops[i][1];
+    P[i].v = ops[i][2];
+    P[i].o = const_cast<void*>(ops[i][3]);
+    P[i].dkp = widths[i][0];
+    P[i].dvp = widths[i][1];
+    P[i].rev = i > 0;
+    P[i].parts = (P[i].dkp + kPartWidth - 1) / kPartWidth;
+    if (P[i].parts > kMaxParts) return cudaErrorNotSupported;
+  }
   const bool want_state[3] = {state_in != nullptr, dstate != nullptr, dstate != nullptr};
   const size_t st_bytes = sizeof(float) * (size_t)BH * dk * dv;
-  size_t bytes = 0, off_in[3], off_ws[3], off_out = 0;
+  size_t bytes = 0, off_in[3], off_ws[3][kMaxParts], off_part[3][kMaxParts], off_out = 0;
   for (int i = 0; i < 3; ++i) {
-    if (!chunk_tc_plan(B, H, N, P[i].dkp, P[i].dvp, chunk, share, &P[i].plan)) return cudaErrorNotSupported;
     off_in[i] = bytes;
     bytes += want_state[i] ? align256(st_bytes) : 0;
-    off_ws[i] = bytes;
-    bytes += align256(P[i].plan.workspace_bytes);
+    for (int j = 0; j < P[i].parts; ++j) {
+      const int w = std::min(kPartWidth, P[i].dkp - j * kPartWidth);
+      if (!chunk_tc_plan(B, H, N, w, P[i].dvp, chunk, share, &P[i].plan[j])) return cudaErrorNotSupported;
+      off_ws[i][j] = bytes;
+      bytes += align256(P[i].plan[j].workspace_bytes);
+      off_part[i][j] = bytes;
+      bytes += j > 0 ? align256((size_t)BH * N * P[i].dvp * 2) : 0;
+    }
   }
   if (dstate_in) {
     off_out = bytes;
@@ -217,7 +264,10 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
   }
   for (int i = 0; i < 3; ++i) {
     P[i].state_in = want_state[i] ? reinterpret_cast<float*>(base + off_in[i]) : nullptr;
-    P[i].ws = P[i].plan.workspace_bytes ? reinterpret_cast<float*>(base + off_ws[i]) : nullptr;
+    for (int j = 0; j < P[i].parts; ++j) {
+      P[i].ws[j] = P[i].plan[j].workspace_bytes ? reinterpret_cast<float*>(base + off_ws[i][j]) : nullptr;
+      P[i].partial[j] = j > 0 ? reinterpret_cast<__nv_bfloat16*>(base + off_part[i][j]) : nullptr;
+    }
   }
   if (dstate_in) P[2].state_out = reinterpret_cast<float*>(base + off_out);
 
@@ -252,9 +302,24 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
       forked[i] = e == cudaSuccess;
     }
     const cudaStream_t where[3] = {s, forked[0] ? a->st[0] : s, forked[1] ? a->st[1] : s};
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = launch_chunk_tc(P[i].q, P[i].k, P[i].v, gamma, P[i].state_in, P[i].o, P[i].state_out, B, H, N, P[i].dkp,
-                          P[i].dvp, P[i].plan, P[i].ws, nullptr, scale, where[i], nullptr, P[i].rev);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+      const Problem& X = P[i];
+      // part j: query/key columns [256 j, 256 j + w) and the same rows of the states
+      for (int j = 0; j < X.parts && e == cudaSuccess; ++j) {
+        const int c0 = j * kPartWidth, w = std::min(kPartWidth, X.dkp - c0);
+        const size_t srow = (size_t)c0 * X.dvp;  // first state element of the part's rows in a head
+        e = launch_chunk_tc(static_cast<const __nv_bfloat16*>(X.q) + c0, static_cast<const __nv_bfloat16*>(X.k) + c0,
+                            X.v, gamma, X.state_in ? X.state_in + srow : nullptr, j == 0 ? X.o : X.partial[j],
+                            X.state_out ? X.state_out + srow : nullptr, B, H, N, w, X.dvp, X.plan[j], X.ws[j], nullptr,
+                            scale, where[i], nullptr, X.rev, X.dkp, (size_t)X.dkp * X.dvp);
+      }
+      for (int j = 1; j < X.parts && e == cudaSuccess; ++j) {
+        const size_t n8 = (size_t)BH * N * X.dvp / 8;
+        const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
+        add_bf16_kernel<<<blocks, 256, 0, where[i]>>>(static_cast<__nv_bfloat16*>(X.o), X.partial[j], n8);
+        e = cudaGetLastError();
+      }
+    }
     // join whatever was forked, whether or not every launch went in
     for (int i = 0; i < 2; ++i) {
       if (!forked[i]) continue;
@@ -299,9 +364,13 @@ int backward_tc_launches(int B, int H, int N, int dk, int dv, bool has_state_in,
   if (has_dstate) n += 1;
   const int w[3][2] = {{dv, dk}, {dv, dk}, {dk, dv}};
   for (int i = 0; i < 3; ++i) {
-    ChunkPlan plan;
-    if (!chunk_tc_plan(B, H, N, w[i][0], w[i][1], chunk, share, &plan)) return -1;
-    n += chunk_tc_launch_count(plan);
+    const int parts = (w[i][0] + kPartWidth - 1) / kPartWidth;
+    for (int j = 0; j < parts; ++j) {
+      ChunkPlan plan;
+      if (!chunk_tc_plan(B, H, N, std::min(kPartWidth, w[i][0] - j * kPartWidth), w[i][1], chunk, share, &plan))
+        return -1;
+      n += chunk_tc_launch_count(plan) + (j > 0 ? 1 : 0);  // a part after the first adds its sum
+    }
   }
   return n;
 }

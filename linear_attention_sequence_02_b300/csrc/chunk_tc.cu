@@ -209,6 +209,7 @@ struct TcParams {
   unsigned int test_stall_us;  // > 0: failure-path test (see retention_test_stall_waits)
   const float* theta;  // rotation kernels: frequencies [dk/2] of the position phase rotation
   int n0;              //   and the position of token 0
+  size_t st_head;      // elements between the heads of state_in and state_out (dk dv when packed)
 };
 
 // Position of this CTA.  Units u = (b*H+h) * n_dv_tiles + value tile.  The
@@ -435,7 +436,7 @@ __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, u
   if (to_out) {
     __syncthreads();
     const float4* src = reinterpret_cast<const float4*>(sm);
-    float* base = p.state_out + (size_t)bh * p.dk * p.dv + dv0;
+    float* base = p.state_out + (size_t)bh * p.st_head + dv0;
     const int cols4 = min(DVT, p.dv - dv0) / 4;  // value columns of this tile inside dv
     for (int q4 = threadIdx.x; q4 < p.dk * cols4; q4 += blockDim.x) {
       const int row = q4 / cols4, c4 = q4 % cols4;
@@ -558,7 +559,8 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           // (rows past dk and columns past dv are padding: they stay zero)
           const float f = gamma_pow(g, lg, (float)seg * seg_len - pad);
           const int col = dv0 + cb * 32;
-          const float4* src = reinterpret_cast<const float4*>(p.state_in + ((size_t)bh * p.dk + row) * p.dv + col);
+          const float4* src =
+              reinterpret_cast<const float4*>(p.state_in + (size_t)bh * p.st_head + (size_t)row * p.dv + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 x = col + 4 * j < p.dv ? __ldg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1369,11 +1371,12 @@ EncodeTiledFn encode_fn() {
 }
 
 // [BH][N][d] bf16 tensor viewed in 3-D with 64-column x `rows`-row boxes, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows) {
+bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows, int ld) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  if (ld <= 0) ld = d;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * (cuuint64_t)N};
   cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -1586,7 +1589,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const float* state_in, void* out, float* state_out, int B, int H, int N,
                             int dk, int dv, const ChunkPlan& plan, float* workspace,
                             const ChunkNorm* norm, float scale, cudaStream_t s, const ChunkRotation* rot,
-                            bool rev) {
+                            bool rev, int ldqk, size_t st_head) {
   const int BH = B * H;
   const int chunk = plan.chunk;
   if (rev && (norm || rot)) return cudaErrorNotSupported;
@@ -1594,7 +1597,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   if (norm && (plan.n_dv_tiles != 1 || plan.dvt != dv)) return cudaErrorNotSupported;
   if (norm && rot) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, q, dk, N, BH, chunk) || !make_map(&mk, k, dk, N, BH, chunk) ||
+  if (!make_map(&mq, q, dk, N, BH, chunk, ldqk) || !make_map(&mk, k, dk, N, BH, chunk, ldqk) ||
       !make_map(&mv, v, dv, N, BH, chunk) ||
       !(norm ? make_map_heads(&mo, out, dv, H, N, B, chunk) : make_map(&mo, out, dv, N, BH, chunk)))
     return cudaErrorInvalidValue;
@@ -1602,6 +1605,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.gamma = gamma;
   p.state_in = state_in;
   p.state_out = state_out;
+  p.st_head = st_head ? st_head : (size_t)dk * dv;
   p.ws = workspace;
   p.norm_w = norm ? norm->weight : nullptr;
   p.norm_b = norm ? norm->bias : nullptr;

@@ -36,7 +36,9 @@ cudaError_t launch_chunkwise_f32(const float* q, const float* k, const float* v,
 // ---- tensor-core chunkwise (chunk_tc.cu) --------------------------------------
 // Tensor map of a [BH][N][d] bf16 tensor as 3-D (d, N, BH) with boxes of 64
 // columns x `rows` rows and 128-byte swizzle; boxes past the ends read zeros.
-bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows);
+// ld: elements between rows (0: d, the rows are packed); the map covers the
+// first d columns of each row.
+bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int rows, int ld = 0);
 struct ChunkPlan {
   int chunk;        // tokens per tile (64 or 128, whatever chunk was asked for)
   int dk_tile;      // query/key columns the kernel is built for (128 or 256; dk <= dk_tile)
@@ -80,14 +82,17 @@ struct ChunkRotation {
 // state_in (nullable) is the state before the first token, [B*H][dk][dv];
 // norm (nullable) selects the GroupNorm epilogue; scale multiplies the query
 // (<= 0: 1/sqrt(dk)); rot (nullable) turns q and k by their positions first.
-// rev runs time backwards: out_m = scale sum_{n>=m} gamma^(n-m) (q_m . k_n) v_n
+// ldqk: elements between the rows of q and of k (0: dk; a larger value reads
+// dk columns of wider rows); st_head: elements between the heads of state_in
+// and state_out (0: dk dv; a larger value addresses dk rows of taller states).  rev runs time backwards: out_m = scale sum_{n>=m} gamma^(n-m) (q_m . k_n) v_n
 // + scale gamma^(N-m) q_m state_in, state_out = gamma^N state_in + sum_n
 // gamma^n k_n^T v_n (not with norm or rot).
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H,
                             int N, int dk, int dv, const ChunkPlan& plan, float* workspace,
                             const ChunkNorm* norm, float scale, cudaStream_t s,
-                            const ChunkRotation* rot = nullptr, bool rev = false);
+                            const ChunkRotation* rot = nullptr, bool rev = false, int ldqk = 0,
+                            size_t st_head = 0);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 // Failure-path test setting read by every chunkwise launch (0: off).
 extern std::atomic<unsigned int> g_test_stall_us;
