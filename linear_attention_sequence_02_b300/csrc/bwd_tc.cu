@@ -35,9 +35,10 @@
 // rows split the same way, so the forward of (q, k, v) from S is the sum of
 // the forwards of (q1, k1, v) from S's first rows and (q2, k2, v) from the
 // rest.  Forwards whose query/key width is above 256 (dq's and dk's when
-// dv > 256) run as 256-column parts on the 128-token tiles (read in place
-// with the row stride of the full width), the first part into the gradient,
-// the others into scratch, then summed into it.
+// dv > 256) run as 256-column parts on the 128-token tiles (q and k read in
+// place with the row stride of the full width; each part's rows of the
+// starting and final states copied to and from packed buffers), the first
+// part into the gradient, the others into scratch, then summed into it.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -183,6 +184,8 @@ struct Problem {
   float* state_out; // or NULL
   float* ws[kMaxParts];
   __nv_bfloat16* partial[kMaxParts];  // outputs of parts 1.. (part 0 writes o)
+  float* part_in[kMaxParts];   // with several parts: each part's rows of the states, packed per head
+  float* part_out[kMaxParts];
 };
 
 // dst += src, bf16, n elements (a multiple of 8, both 16-byte aligned).
@@ -253,6 +256,19 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
       bytes += j > 0 ? align256((size_t)BH * N * P[i].dvp * 2) : 0;
     }
   }
+  // packed per-part state rows (only for problems in several parts)
+  size_t off_pin[3][kMaxParts] = {}, off_pout[3][kMaxParts] = {};
+  for (int i = 0; i < 3; ++i) {
+    if (P[i].parts < 2) continue;
+    for (int j = 0; j < P[i].parts; ++j) {
+      const size_t w = (size_t)std::min(kPartWidth, P[i].dkp - j * kPartWidth);
+      const size_t pb = sizeof(float) * (size_t)BH * w * P[i].dvp;
+      off_pin[i][j] = bytes;
+      bytes += want_state[i] ? align256(pb) : 0;
+      off_pout[i][j] = bytes;
+      bytes += (i == 2 && dstate_in) ? align256(pb) : 0;
+    }
+  }
   if (dstate_in) {
     off_out = bytes;
     bytes += align256(st_bytes);
@@ -267,6 +283,9 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
     for (int j = 0; j < P[i].parts; ++j) {
       P[i].ws[j] = P[i].plan[j].workspace_bytes ? reinterpret_cast<float*>(base + off_ws[i][j]) : nullptr;
       P[i].partial[j] = j > 0 ? reinterpret_cast<__nv_bfloat16*>(base + off_part[i][j]) : nullptr;
+      const bool multi = P[i].parts > 1;
+      P[i].part_in[j] = multi && want_state[i] ? reinterpret_cast<float*>(base + off_pin[i][j]) : nullptr;
+      P[i].part_out[j] = multi && i == 2 && dstate_in ? reinterpret_cast<float*>(base + off_pout[i][j]) : nullptr;
     }
   }
   if (dstate_in) P[2].state_out = reinterpret_cast<float*>(base + off_out);
@@ -307,11 +326,26 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
       // part j: query/key columns [256 j, 256 j + w) and the same rows of the states
       for (int j = 0; j < X.parts && e == cudaSuccess; ++j) {
         const int c0 = j * kPartWidth, w = std::min(kPartWidth, X.dkp - c0);
-        const size_t srow = (size_t)c0 * X.dvp;  // first state element of the part's rows in a head
-        e = launch_chunk_tc(static_cast<const __nv_bfloat16*>(X.q) + c0, static_cast<const __nv_bfloat16*>(X.k) + c0,
-                            X.v, gamma, X.state_in ? X.state_in + srow : nullptr, j == 0 ? X.o : X.partial[j],
-                            X.state_out ? X.state_out + srow : nullptr, B, H, N, w, X.dvp, X.plan[j], X.ws[j], nullptr,
-                            scale, where[i], nullptr, X.rev, X.dkp, (size_t)X.dkp * X.dvp);
+        // a part's rows of a head's state: w rows of dvp floats at row c0 of the dkp-row state
+        const size_t head = sizeof(float) * (size_t)X.dkp * X.dvp, rows = sizeof(float) * (size_t)w * X.dvp;
+        const size_t first = sizeof(float) * (size_t)c0 * X.dvp;
+        const float* sin = X.state_in;
+        float* sout = X.state_out;
+        if (X.parts > 1) {
+          if (X.state_in) {
+            e = cudaMemcpy2DAsync(X.part_in[j], rows, reinterpret_cast<const char*>(X.state_in) + first, head, rows,
+                                  BH, cudaMemcpyDeviceToDevice, where[i]);
+            sin = X.part_in[j];
+          }
+          sout = X.part_out[j];
+        }
+        if (e == cudaSuccess)
+          e = launch_chunk_tc(static_cast<const __nv_bfloat16*>(X.q) + c0, static_cast<const __nv_bfloat16*>(X.k) + c0,
+                              X.v, gamma, sin, j == 0 ? X.o : X.partial[j], sout, B, H, N, w, X.dvp, X.plan[j],
+                              X.ws[j], nullptr, scale, where[i], nullptr, X.rev, X.dkp);
+        if (e == cudaSuccess && X.parts > 1 && X.state_out)
+          e = cudaMemcpy2DAsync(reinterpret_cast<char*>(X.state_out) + first, head, X.part_out[j], rows, rows, BH,
+                                cudaMemcpyDeviceToDevice, where[i]);
       }
       for (int j = 1; j < X.parts && e == cudaSuccess; ++j) {
         const size_t n8 = (size_t)BH * N * X.dvp / 8;

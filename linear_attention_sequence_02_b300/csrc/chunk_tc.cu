@@ -209,7 +209,6 @@ struct TcParams {
   unsigned int test_stall_us;  // > 0: failure-path test (see retention_test_stall_waits)
   const float* theta;  // rotation kernels: frequencies [dk/2] of the position phase rotation
   int n0;              //   and the position of token 0
-  size_t st_head;      // elements between the heads of state_in and state_out (dk dv when packed)
 };
 
 // Position of this CTA.  Units u = (b*H+h) * n_dv_tiles + value tile.  The
@@ -436,7 +435,7 @@ __device__ __noinline__ void write_final_state(const TcParams& p, uint8_t* sm, u
   if (to_out) {
     __syncthreads();
     const float4* src = reinterpret_cast<const float4*>(sm);
-    float* base = p.state_out + (size_t)bh * p.st_head + dv0;
+    float* base = p.state_out + (size_t)bh * p.dk * p.dv + dv0;
     const int cols4 = min(DVT, p.dv - dv0) / 4;  // value columns of this tile inside dv
     for (int q4 = threadIdx.x; q4 < p.dk * cols4; q4 += blockDim.x) {
       const int row = q4 / cols4, c4 = q4 % cols4;
@@ -559,8 +558,7 @@ __device__ __forceinline__ void chunk_roles(const TcParams& p, const RoleCtx& x)
           // (rows past dk and columns past dv are padding: they stay zero)
           const float f = gamma_pow(g, lg, (float)seg * seg_len - pad);
           const int col = dv0 + cb * 32;
-          const float4* src =
-              reinterpret_cast<const float4*>(p.state_in + (size_t)bh * p.st_head + (size_t)row * p.dv + col);
+          const float4* src = reinterpret_cast<const float4*>(p.state_in + ((size_t)bh * p.dk + row) * p.dv + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 x = col + 4 * j < p.dv ? __ldg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1589,7 +1587,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const float* state_in, void* out, float* state_out, int B, int H, int N,
                             int dk, int dv, const ChunkPlan& plan, float* workspace,
                             const ChunkNorm* norm, float scale, cudaStream_t s, const ChunkRotation* rot,
-                            bool rev, int ldqk, size_t st_head) {
+                            bool rev, int ldqk) {
   const int BH = B * H;
   const int chunk = plan.chunk;
   if (rev && (norm || rot)) return cudaErrorNotSupported;
@@ -1605,7 +1603,6 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
   p.gamma = gamma;
   p.state_in = state_in;
   p.state_out = state_out;
-  p.st_head = st_head ? st_head : (size_t)dk * dv;
   p.ws = workspace;
   p.norm_w = norm ? norm->weight : nullptr;
   p.norm_b = norm ? norm->bias : nullptr;

@@ -83,16 +83,14 @@ struct ChunkRotation {
 // norm (nullable) selects the GroupNorm epilogue; scale multiplies the query
 // (<= 0: 1/sqrt(dk)); rot (nullable) turns q and k by their positions first.
 // ldqk: elements between the rows of q and of k (0: dk; a larger value reads
-// dk columns of wider rows); st_head: elements between the heads of state_in
-// and state_out (0: dk dv; a larger value addresses dk rows of taller states).  rev runs time backwards: out_m = scale sum_{n>=m} gamma^(n-m) (q_m . k_n) v_n
+// dk columns of wider rows).  rev runs time backwards: out_m = scale sum_{n>=m} gamma^(n-m) (q_m . k_n) v_n
 // + scale gamma^(N-m) q_m state_in, state_out = gamma^N state_in + sum_n
 // gamma^n k_n^T v_n (not with norm or rot).
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* gamma,
                             const float* state_in, void* out, float* state_out, int B, int H,
                             int N, int dk, int dv, const ChunkPlan& plan, float* workspace,
                             const ChunkNorm* norm, float scale, cudaStream_t s,
-                            const ChunkRotation* rot = nullptr, bool rev = false, int ldqk = 0,
-                            size_t st_head = 0);
+                            const ChunkRotation* rot = nullptr, bool rev = false, int ldqk = 0);
 cudaError_t read_device_status(unsigned int* flags, int clear);
 // Failure-path test setting read by every chunkwise launch (0: off).
 extern std::atomic<unsigned int> g_test_stall_us;
