@@ -109,6 +109,8 @@ def test_backward_launch_counts(lib):
     assert f(4, 8, 2048, 128, 128, 0, 0, 0, ctypes.byref(n)) == binding.RET_OK and n.value == 3
     assert f(4, 8, 2048, 128, 128, 1, 1, 1, ctypes.byref(n)) == binding.RET_OK and n.value == 6
     assert f(1, 16, 16384, 128, 256, 0, 0, 0, ctypes.byref(n)) == binding.RET_OK and n.value >= 4
+    # the 7B widths: dq's and dk's forwards in two 256-column parts each, plus their sums
+    assert f(8, 16, 8192, 256, 512, 0, 0, 0, ctypes.byref(n)) == binding.RET_OK and n.value >= 3 * 1 + 2 * 2
     assert f(1, 2, 100, 40, 24, 1, 1, 1, ctypes.byref(n)) == binding.RET_OK and n.value == 1
     assert f(1, 2, 0, 128, 128, 0, 0, 1, ctypes.byref(n)) == binding.RET_OK and n.value == 1
     assert f(0, 2, 10, 128, 128, 0, 0, 1, ctypes.byref(n)) == binding.RET_ERR_INVALID
