@@ -55,6 +55,8 @@ def _check(orc, q, k, v, g, dout, s0, ds, tol, f32=False, what=""):
     (1, 3, 333, 48, 80, False),     # tensor cores, widths padded to the tiles
     (1, 2, 300, 256, 512, True),    # tensor cores, the 7B widths: dq's and dk's forwards have 512-wide queries
     (1, 2, 1100, 512, 128, True),   # tensor cores, d_k = 512: the dv forward's queries, segments
+    (1, 60, 2048, 64, 64, True),    # tensor cores, more heads than a third of the SMs: the time-reversed
+                                    # forwards cut their last wave's heads into segments
 ])
 def test_backward_matches_oracle(orc, B, H, N, dk, dv, states):
     q, k, v, dout, s0, ds = _case(B, H, N, dk, dv, 5, torch.bfloat16, states)

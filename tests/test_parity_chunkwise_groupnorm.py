@@ -33,6 +33,7 @@ def _affine(H, dv, seed):
     (1, 2, 300, 256, 128, 128),   # d_k = 256
     (1, 2, 333, 256, 64, 64),
     (4, 8, 2048, 128, 128, 64),   # the mid workload
+    (2, 80, 1024, 64, 64, 64),    # more heads than SMs: the last wave's heads cut into segments
 ])
 def test_chunkwise_groupnorm_matches_oracle(orc, B, H, N, dk, dv, C):
     q, k, v = inputs.qkv(B, H, N, dk, dv, 11, torch.bfloat16)

@@ -28,13 +28,14 @@ def oracle_rotated(orc, q, k, v, g, th, n0, C, s0=None):
 
 
 @pytest.mark.parametrize("B,H,N,dk,dv,C,n0", [
-    (1, 2, 300, 128, 128, 64, 0),      # lookahead variant, ragged tail
-    (2, 2, 333, 128, 256, 128, 17),    # chunk 128, two value tiles, start position 17
+    (1, 2, 300, 128, 128, 64, 0),      # ragged tail
+    (2, 2, 333, 128, 256, 128, 17),    # two value tiles (q, k turned by a separate pass), start position 17
     (1, 2, 300, 256, 128, 64, 5),      # d_k 256: two halves per chunk
     (1, 2, 400, 256, 128, 128, 0),     # d_k 256, chunk 128 (one chunk of Q/K in the ring)
     (1, 3, 250, 64, 96, 64, 1000),     # widths padded to the tiles
-    (1, 2, 2048, 128, 128, 64, 3),     # segments: the state-only pre-pass turns the keys
+    (1, 2, 2048, 128, 128, 64, 3),     # segments on 64-token tiles: the state-only pre-pass turns the keys
     (1, 1, 3000, 256, 64, 128, 77),    # segments with d_k 256
+    (2, 80, 1024, 64, 64, 64, 9),      # more heads than SMs: the last wave's heads cut into segments
 ])
 def test_chunkwise_rotated_matches_oracle(orc, B, H, N, dk, dv, C, n0):
     q, k, v = inputs.qkv(B, H, N, dk, dv, 31, torch.bfloat16)
